@@ -1,0 +1,110 @@
+"""CPU oracle for grouped-query decode attention (fp64, plain loops in C).
+
+TEST INFRASTRUCTURE ONLY: the test suite, the package smoke check and the
+bench's CPU-baseline / reference arm may import this module; the GPU path never
+does, and shares no code with it. See gqa_oracle.c for the definition it
+follows ("GQA analysis", section "Grouped broadcast"; bottom-right causal mask
+for several new tokens per the mask-handling part of section 7 of "Same GQA,
+Different Execution Cost Across Backends").
+
+Every function here is pinned by the `-m "not gpu"` tests in tests/ against
+facts that do not come from the oracle itself (the head-mapping table printed
+on the first page, repeat_kv / repeat_interleave expansion, PyTorch's own
+scaled_dot_product_attention in float64, high-precision brute force, closed
+forms); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "gqa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle_gqa.so")
+_lock = threading.Lock()
+_default = None
+
+
+def compile_oracle(src: str, out_path: str) -> str:
+    """Plain gcc build of an oracle source file into a shared library."""
+    tmp = out_path + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", src, "-o", tmp, "-lm"])
+    os.replace(tmp, out_path)
+    return out_path
+
+
+def build(force: bool = False) -> str:
+    if force or not os.path.exists(_LIB_PATH) or (
+        os.path.getmtime(_LIB_PATH) < os.path.getmtime(SOURCE)
+    ):
+        compile_oracle(SOURCE, _LIB_PATH)
+    return _LIB_PATH
+
+
+class Oracle:
+    """ctypes handle on one build of the oracle (the real one, or a test's
+    deliberately broken copy)."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        vp, i32, lng = ctypes.c_void_p, ctypes.c_int, ctypes.c_long
+        lib.oracle_gqa_decode_f64.argtypes = [vp, vp, vp, vp, ctypes.c_double,
+                                              i32, i32, i32, i32, i32, i32, lng, lng, vp, vp]
+        lib.oracle_gqa_decode_f64.restype = ctypes.c_int
+        self._lib = lib
+        self.path = lib_path
+
+    def gqa_decode(self, q, k, v, seq_lens, scale, rows=None, threads: int = 1):
+        """q [B,sq,H,D], k/v [B,G,Tmax,D] as bf16 bit arrays (uint16); seq_lens [B].
+
+        Returns (out [B,sq,H,D] float64, lse [B,sq,H] float64). With `rows`
+        = (begin, end) only those flat rows r = (b*sq+s)*H+h are computed; the
+        others are left NaN. `threads` splits the rows over host threads (each
+        row is still computed by one thread in index order, so the result does
+        not depend on the split)."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        k = np.ascontiguousarray(k, dtype=np.uint16)
+        v = np.ascontiguousarray(v, dtype=np.uint16)
+        lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        B, sq, H, D = q.shape
+        Bk, G, Tmax, Dk = k.shape
+        if (Bk, Dk) != (B, D) or v.shape != k.shape or lens.shape != (B,):
+            raise ValueError("shape mismatch")
+        out = np.full((B, sq, H, D), np.nan)
+        lse = np.full((B, sq, H), np.nan)
+        nrows = B * sq * H
+        r0, r1 = (0, nrows) if rows is None else rows
+        threads = max(1, min(int(threads), r1 - r0 if r1 > r0 else 1))
+        bounds = [r0 + ((r1 - r0) * i) // threads for i in range(threads + 1)]
+
+        def work(i):
+            return self._lib.oracle_gqa_decode_f64(
+                q.ctypes.data, k.ctypes.data, v.ctypes.data, lens.ctypes.data, float(scale),
+                B, sq, H, G, D, Tmax, bounds[i], bounds[i + 1], out.ctypes.data, lse.ctypes.data)
+
+        if threads == 1:
+            rcs = [work(0)]
+        else:
+            with ThreadPoolExecutor(threads) as ex:
+                rcs = list(ex.map(work, range(threads)))
+        if any(rc != 0 for rc in rcs):
+            raise ValueError("oracle rejected the arguments")
+        return out, lse
+
+
+def get() -> Oracle:
+    """The oracle built from gqa_oracle.c (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def gqa_decode_f64(q, k, v, seq_lens, scale, rows=None, threads: int = 1):
+    return get().gqa_decode(q, k, v, seq_lens, scale, rows=rows, threads=threads)
