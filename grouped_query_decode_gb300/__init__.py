@@ -1,0 +1,164 @@
+"""GB300 (sm_103a) grouped-query decode attention.
+
+A thin ctypes binding over the C ABI of libgqa_decode.so (include/gqa_decode.h):
+the functions here only check and marshal arguments -- every step of the
+computation runs in the library's CUDA kernels. There is no CPU fallback: if
+the library cannot be built or loaded, every call raises.
+
+    out, lse = torch.empty(...), torch.empty(...)
+    gqa_decode(q, k_cache, v_cache, seq_lens, scale, out, lse)
+
+q [B, sq, H, D], k_cache / v_cache [B, G, Tmax, D] and out are bfloat16 CUDA
+tensors; seq_lens [B] is int32 on the same device; lse [B, sq, H] float32 or
+None. Calls are enqueued on the current torch CUDA stream (or `stream`).
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from . import build as _build
+
+GQA_OK = 0
+GQA_ERR_INVALID_ARG = -1
+GQA_ERR_HEAD_RATIO = -2
+GQA_ERR_UNSUPPORTED = -3
+GQA_ERR_MISALIGNED = -4
+GQA_ERR_WORKSPACE = -5
+GQA_ERR_CUDA = -6
+GQA_ERR_DEVICE_TIMEOUT = -7
+
+LIB_PATH = _build.LIB_PATH
+_lib = None
+_lock = threading.Lock()
+
+
+class GQADecodeError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = strerror(status) if _lib is not None else str(status)
+        if status == GQA_ERR_CUDA and _lib is not None:
+            msg += f" (cudaError {gqa_decode_last_cuda_error()})"
+        super().__init__(f"{what}: {msg}" if what else msg)
+
+
+class PlanT(ctypes.Structure):
+    _fields_ = [("ctas", ctypes.c_int), ("tile_tokens", ctypes.c_int),
+                ("row_tiles", ctypes.c_int), ("stages", ctypes.c_int),
+                ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int),
+                ("max_tiles", ctypes.c_longlong)]
+
+
+def load():
+    """Builds (if the sources are newer) and loads libgqa_decode.so."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            lib = ctypes.CDLL(path)
+            vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            shape = [i32] * 6
+            lib.gqa_decode.argtypes = [vp, vp, vp, vp, f32, vp, vp, *shape, vp]
+            lib.gqa_decode.restype = i32
+            lib.gqa_decode_ex.argtypes = [vp, vp, vp, vp, f32, vp, vp, *shape, vp, sz, vp]
+            lib.gqa_decode_ex.restype = i32
+            lib.gqa_decode_workspace_bytes.argtypes = shape
+            lib.gqa_decode_workspace_bytes.restype = sz
+            lib.gqa_decode_plan.argtypes = [*shape, i32, ctypes.POINTER(PlanT)]
+            lib.gqa_decode_plan.restype = i32
+            lib.gqa_decode_check_error.argtypes = [vp]
+            lib.gqa_decode_check_error.restype = i32
+            lib.gqa_decode_last_cuda_error.argtypes = []
+            lib.gqa_decode_last_cuda_error.restype = i32
+            lib.gqa_decode_strerror.argtypes = [i32]
+            lib.gqa_decode_strerror.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return load().gqa_decode_strerror(int(status)).decode()
+
+
+def gqa_decode_strerror(status: int) -> str:
+    return strerror(status)
+
+
+def gqa_decode_last_cuda_error() -> int:
+    return int(load().gqa_decode_last_cuda_error())
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _shapes(q, k_cache, v_cache, seq_lens, out, lse):
+    import torch
+    for name, t, dt in (("q", q, torch.bfloat16), ("k_cache", k_cache, torch.bfloat16),
+                        ("v_cache", v_cache, torch.bfloat16), ("seq_lens", seq_lens, torch.int32),
+                        ("out", out, torch.bfloat16)):
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous()):
+        raise TypeError("lse must be a contiguous float32 CUDA tensor or None")
+    if q.dim() != 4 or k_cache.dim() != 4:
+        raise ValueError("q is [B, sq, H, D] and k_cache [B, G, Tmax, D]")
+    B, sq, H, D = q.shape
+    Bk, G, Tmax, Dk = k_cache.shape
+    if (Bk, Dk) != (B, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache / v_cache must be [B, G, Tmax, D] with q's B and D")
+    if tuple(seq_lens.shape) != (B,) or tuple(out.shape) != (B, sq, H, D):
+        raise ValueError("seq_lens must be [B] and out [B, sq, H, D]")
+    if lse is not None and tuple(lse.shape) != (B, sq, H):
+        raise ValueError("lse must be [B, sq, H]")
+    return B, sq, H, G, D, Tmax
+
+
+def gqa_decode(q, k_cache, v_cache, seq_lens, scale, out, lse=None, stream=None):
+    """One decode step (library-owned workspace). See include/gqa_decode.h."""
+    B, sq, H, G, D, Tmax = _shapes(q, k_cache, v_cache, seq_lens, out, lse)
+    rc = load().gqa_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                           seq_lens.data_ptr(), float(scale), out.data_ptr(),
+                           None if lse is None else lse.data_ptr(), B, sq, H, G, D, Tmax,
+                           _stream_handle(stream, q.device))
+    if rc != GQA_OK:
+        raise GQADecodeError(rc, "gqa_decode")
+
+
+def gqa_decode_ex(q, k_cache, v_cache, seq_lens, scale, out, lse, workspace, stream=None):
+    """One decode step with a caller-owned workspace (a CUDA uint8 tensor of at
+    least gqa_decode_workspace_bytes(...) bytes)."""
+    B, sq, H, G, D, Tmax = _shapes(q, k_cache, v_cache, seq_lens, out, lse)
+    rc = load().gqa_decode_ex(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                              seq_lens.data_ptr(), float(scale), out.data_ptr(),
+                              None if lse is None else lse.data_ptr(), B, sq, H, G, D, Tmax,
+                              workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                              _stream_handle(stream, q.device))
+    if rc != GQA_OK:
+        raise GQADecodeError(rc, "gqa_decode_ex")
+
+
+def gqa_decode_workspace_bytes(B, sq, H, G, D, Tmax) -> int:
+    return int(load().gqa_decode_workspace_bytes(B, sq, H, G, D, Tmax))
+
+
+def gqa_decode_plan(B, sq, H, G, D, Tmax, num_sms) -> dict:
+    plan = PlanT()
+    rc = load().gqa_decode_plan(B, sq, H, G, D, Tmax, num_sms, ctypes.byref(plan))
+    if rc != GQA_OK:
+        raise GQADecodeError(rc, "gqa_decode_plan")
+    return {f: getattr(plan, f) for f, _ in PlanT._fields_}
+
+
+def gqa_decode_check_error(stream=None, device=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status."""
+    import torch
+    dev = device if device is not None else torch.cuda.current_device()
+    return int(load().gqa_decode_check_error(_stream_handle(stream, dev)))

@@ -1,0 +1,285 @@
+// C ABI of libgqa_decode.so: argument checks, the work plan, TMA descriptors,
+// workspace management and kernel launches. See include/gqa_decode.h for the
+// contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "gqa_decode.h"
+#include "gqa_launch.h"
+
+namespace {
+
+using namespace gqa;
+
+// Status word the kernels set when a bounded wait expires; one per device.
+__device__ unsigned int g_status_word;
+
+thread_local int t_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    t_last_cuda_error = (int)e;
+    return GQA_ERR_CUDA;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    unsigned* status = nullptr;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_devices;
+std::map<std::pair<int, cudaStream_t>, std::pair<void*, size_t>> g_workspaces;
+
+int device_info(DeviceInfo* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_devices.find(dev);
+    if (it == g_devices.end()) {
+        DeviceInfo info;
+        e = cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        void* sym = nullptr;
+        e = cudaGetSymbolAddress(&sym, g_status_word);
+        if (e != cudaSuccess) return cuda_fail(e);
+        info.status = static_cast<unsigned*>(sym);
+        it = g_devices.emplace(dev, info).first;
+    }
+    *out = it->second;
+    return GQA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// A [B*G units][Tmax][D] bf16 cache viewed as a 3-D tensor; boxes of 64 rows x
+// 64 elements (128 bytes) with the 128-byte swizzle. Rows past Tmax read as 0.
+int encode_cache_map(CUtensorMap* map, const void* base, int B, int G, int Tmax, int D) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return cuda_fail(cudaErrorNotSupported);
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Tmax, (cuuint64_t)B * G};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Tmax * D * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kBoxCols, (cuuint32_t)kTileTokens, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+    return GQA_OK;
+}
+
+int check_shapes(int B, int sq, int H, int G, int D, int Tmax) {
+    if (B <= 0 || sq <= 0 || H <= 0 || G <= 0 || D <= 0 || Tmax <= 0) return GQA_ERR_INVALID_ARG;
+    if (H % G != 0) return GQA_ERR_HEAD_RATIO;
+    if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
+    const long long R = (long long)(H / G) * sq;
+    if (R > 16 * kMaxRowTiles) return GQA_ERR_UNSUPPORTED;
+    // Index arithmetic in the kernels uses 32-bit row numbers and coordinates.
+    if ((long long)B * sq * H >= (1ll << 31) || (long long)B * G >= (1ll << 31))
+        return GQA_ERR_UNSUPPORTED;
+    return GQA_OK;
+}
+
+// Smallest share of tiles worth giving a CTA. The default (4 tiles, 256
+// tokens) keeps small problems from being cut into one-tile partials; the
+// environment variable exists for sweeps of the plan and for tests that want
+// many splits on small inputs.
+int min_tiles_per_cta() {
+    const char* s = std::getenv("GQA_DECODE_MIN_TILES_PER_CTA");
+    const int x = s ? std::atoi(s) : 0;
+    return x > 0 ? x : 4;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int gqa_decode_plan(int B, int sq, int H, int G, int D, int Tmax, int num_sms,
+                    gqa_decode_plan_t* plan) {
+    if (!plan || num_sms <= 0) return GQA_ERR_INVALID_ARG;
+    int st = check_shapes(B, sq, H, G, D, Tmax);
+    if (st != GQA_OK) return st;
+    const int R = (H / G) * sq;
+    const int mt = (R + 15) / 16;
+    const long long tiles_per_unit = (Tmax + kTileTokens - 1) / kTileTokens;
+    const long long max_tiles = (long long)B * G * tiles_per_unit;
+    long long ctas = (max_tiles + min_tiles_per_cta() - 1) / min_tiles_per_cta();
+    if (ctas > num_sms) ctas = num_sms;
+    if (ctas < 1) ctas = 1;
+    plan->ctas = (int)ctas;
+    plan->tile_tokens = kTileTokens;
+    plan->row_tiles = mt;
+    plan->stages = splitkv_stages(D, mt);
+    plan->threads = splitkv_threads(D, mt);
+    plan->smem_bytes = splitkv_smem_bytes(D, mt);
+    plan->max_tiles = max_tiles;
+    return GQA_OK;
+}
+
+size_t gqa_decode_workspace_bytes(int B, int sq, int H, int G, int D, int Tmax) {
+    DeviceInfo info;
+    if (device_info(&info) != GQA_OK) return 0;
+    gqa_decode_plan_t plan;
+    if (gqa_decode_plan(B, sq, H, G, D, Tmax, info.sms, &plan) != GQA_OK) return 0;
+    return ws_total_bytes(B, (H / G) * sq, D, plan.ctas);
+}
+
+int gqa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* seq_lens, float scale, void* out, float* lse, int B, int sq,
+                  int H, int G, int D, int Tmax, void* workspace, size_t workspace_bytes,
+                  cudaStream_t stream) {
+    if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_INVALID_ARG;
+    int st = check_shapes(B, sq, H, G, D, Tmax);
+    if (st != GQA_OK) return st;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(seq_lens) ||
+        !aligned16(out) || (lse && !aligned16(lse)))
+        return GQA_ERR_MISALIGNED;
+    DeviceInfo info;
+    st = device_info(&info);
+    if (st != GQA_OK) return st;
+    gqa_decode_plan_t plan;
+    st = gqa_decode_plan(B, sq, H, G, D, Tmax, info.sms, &plan);
+    if (st != GQA_OK) return st;
+    const int R = (H / G) * sq;
+    const size_t need = ws_total_bytes(B, R, D, plan.ctas);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return GQA_ERR_WORKSPACE;
+
+    LaunchArgs a;
+    st = encode_cache_map(&a.tm_k, k_cache, B, G, Tmax, D);
+    if (st != GQA_OK) return st;
+    st = encode_cache_map(&a.tm_v, v_cache, B, G, Tmax, D);
+    if (st != GQA_OK) return st;
+    a.p.q = static_cast<const uint16_t*>(q);
+    a.p.seq_lens = seq_lens;
+    a.p.out = static_cast<uint16_t*>(out);
+    a.p.lse = lse;
+    a.p.ws_prefix = static_cast<long long*>(workspace);
+    a.p.ws_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws_prefix_bytes(B));
+    a.p.status = info.status;
+    a.p.scale_log2 = scale * 1.4426950408889634f;
+    a.p.B = B;
+    a.p.sq = sq;
+    a.p.H = H;
+    a.p.G = G;
+    a.p.Tmax = Tmax;
+    a.p.R = R;
+    a.p.heads_per_group = H / G;
+    a.p.ctas = plan.ctas;
+    a.row_tiles = plan.row_tiles;
+    a.pdl = true;
+    a.stream = stream;
+    cudaError_t e = D == 64 ? launch_d64(a) : launch_d128(a);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return GQA_OK;
+}
+
+int gqa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
+               float scale, void* out, float* lse, int B, int sq, int H, int G, int D, int Tmax,
+               cudaStream_t stream) {
+    int st = check_shapes(B, sq, H, G, D, Tmax);
+    if (st != GQA_OK) return st;
+    if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_INVALID_ARG;
+    const size_t need = gqa_decode_workspace_bytes(B, sq, H, G, D, Tmax);
+    if (need == 0) return GQA_ERR_CUDA;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    void* ws = nullptr;
+    size_t have = 0;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto& slot = g_workspaces[{dev, stream}];
+        if (slot.second < need) {
+            if (slot.first) {
+                // The old buffer may still be in use by work queued on this stream.
+                e = cudaStreamSynchronize(stream);
+                if (e != cudaSuccess) return cuda_fail(e);
+                cudaFree(slot.first);
+                slot = {nullptr, 0};
+            }
+            void* p = nullptr;
+            e = cudaMalloc(&p, need);
+            if (e != cudaSuccess) return cuda_fail(e);
+            slot = {p, need};
+        }
+        ws = slot.first;
+        have = slot.second;
+    }
+    return gqa_decode_ex(q, k_cache, v_cache, seq_lens, scale, out, lse, B, sq, H, G, D, Tmax, ws,
+                         have, stream);
+}
+
+int gqa_decode_check_error(cudaStream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    DeviceInfo info;
+    int st = device_info(&info);
+    if (st != GQA_OK) return st;
+    unsigned word = 0;
+    e = cudaMemcpy(&word, info.status, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (word) {
+        const unsigned zero = 0;
+        e = cudaMemcpy(info.status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (word & kStatusTimeout) return GQA_ERR_DEVICE_TIMEOUT;
+    }
+    return GQA_OK;
+}
+
+int gqa_decode_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* gqa_decode_strerror(int status) {
+    switch (status) {
+        case GQA_OK: return "ok";
+        case GQA_ERR_INVALID_ARG: return "invalid argument (null pointer or non-positive size)";
+        case GQA_ERR_HEAD_RATIO: return "H is not a multiple of G";
+        case GQA_ERR_UNSUPPORTED: return "unsupported shape (D must be 64 or 128, (H/G)*sq <= 32)";
+        case GQA_ERR_MISALIGNED: return "a tensor pointer is not 16-byte aligned";
+        case GQA_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+        case GQA_ERR_CUDA: return "a CUDA call failed (see gqa_decode_last_cuda_error)";
+        case GQA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait expired";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"
+
+namespace gqa {
+
+int splitkv_smem_bytes(int D, int mt) {
+    if (D == 64) return mt == 1 ? KernelShape<64, 1>::kSmemBytes : KernelShape<64, 2>::kSmemBytes;
+    return mt == 1 ? KernelShape<128, 1>::kSmemBytes : KernelShape<128, 2>::kSmemBytes;
+}
+int splitkv_threads(int D, int mt) {
+    if (D == 64) return mt == 1 ? KernelShape<64, 1>::kThreads : KernelShape<64, 2>::kThreads;
+    return mt == 1 ? KernelShape<128, 1>::kThreads : KernelShape<128, 2>::kThreads;
+}
+int splitkv_stages(int D, int mt) {
+    if (D == 64) return mt == 1 ? KernelShape<64, 1>::kStages : KernelShape<64, 2>::kStages;
+    return mt == 1 ? KernelShape<128, 1>::kStages : KernelShape<128, 2>::kStages;
+}
+
+}  // namespace gqa

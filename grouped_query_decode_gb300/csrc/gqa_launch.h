@@ -1,0 +1,30 @@
+// Internal interface between the C ABI (api.cu) and the kernel translation
+// units (one per head dimension, so that they compile in parallel).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+#include "gqa_common.h"
+
+namespace gqa {
+
+struct LaunchArgs {
+    CUtensorMap tm_k;
+    CUtensorMap tm_v;
+    DecodeParams p;
+    int row_tiles;   // 1 or 2
+    bool pdl;        // launch with programmatic stream serialization
+    cudaStream_t stream;
+};
+
+// Enqueue the split-KV kernel and the combine kernel for D = 64 / D = 128.
+cudaError_t launch_d64(const LaunchArgs& a);
+cudaError_t launch_d128(const LaunchArgs& a);
+
+// Dynamic shared memory and threads per CTA of the split-KV kernel.
+int splitkv_smem_bytes(int D, int row_tiles);
+int splitkv_threads(int D, int row_tiles);
+int splitkv_stages(int D, int row_tiles);
+
+}  // namespace gqa

@@ -1,0 +1,11 @@
+// Kernel instances for head dimension 128.
+#include "gqa_launch_impl.cuh"
+
+namespace gqa {
+
+cudaError_t launch_d128(const LaunchArgs& a) {
+    return a.row_tiles == 1 ? launch_splitkv_and_combine<128, 1>(a)
+                            : launch_splitkv_and_combine<128, 2>(a);
+}
+
+}  // namespace gqa

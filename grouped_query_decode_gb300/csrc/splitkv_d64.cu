@@ -1,0 +1,11 @@
+// Kernel instances for head dimension 64.
+#include "gqa_launch_impl.cuh"
+
+namespace gqa {
+
+cudaError_t launch_d64(const LaunchArgs& a) {
+    return a.row_tiles == 1 ? launch_splitkv_and_combine<64, 1>(a)
+                            : launch_splitkv_and_combine<64, 2>(a);
+}
+
+}  // namespace gqa

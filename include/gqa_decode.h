@@ -1,0 +1,143 @@
+/*
+ * gqa_decode.h -- C ABI of the GB300 (sm_103a) grouped-query decode attention
+ * library, libgqa_decode.so.
+ *
+ * The operation ("GQA analysis", section "Grouped broadcast"): with H query
+ * heads sharing G key/value heads, query head h reads only KV head
+ *     g(h) = floor(h / (H / G)),
+ *     score[h] = softmax(Q[h] . K[g(h)]^T * scale),
+ *     O[h]     = score[h] . V[g(h)].
+ * The page's scale is 1/sqrt(D); here it is an argument. G = H is multi-head
+ * attention and G = 1 is multi-query attention ("Fast Transformer Decoding
+ * with Multi-Query Attention" digest, section "Multi-Query Attention"); H must
+ * be a multiple of G ("keep query heads, cut KV heads", section "three names
+ * on one axis").
+ *
+ * One call is one decode step of one layer: the inner per-head loop of the
+ * incremental decode in "GQA analysis", section "Incremental decode", for
+ * every sequence of the batch. The sq new tokens' K/V must already be appended
+ * to the cache (the page appends before attending), so seq_lens[b] counts them.
+ * For sq > 1 the new tokens are causal among themselves, bottom-right aligned
+ * (the mask-handling part of section 7 of "Same GQA, Different Execution Cost
+ * Across Backends"): new token s sits at absolute position T_b - sq + s and
+ * attends to cache positions t <= T_b - sq + s.
+ *
+ * Layouts (all dense, C-contiguous, device memory, 16-byte aligned):
+ *   q        [B, sq, H, D]    bfloat16
+ *   k_cache  [B, G, Tmax, D]  bfloat16 (the [batch, kv_heads, seq, head_dim]
+ *   v_cache  [B, G, Tmax, D]  bfloat16  cache of "GQA analysis", section 4)
+ *   seq_lens [B]              int32, valid entries per sequence (incl. the new
+ *                             tokens); values are clamped to [0, Tmax] on the
+ *                             device. Entries at t >= seq_lens[b] are never
+ *                             used, whatever they hold.
+ *   out      [B, sq, H, D]    bfloat16, round-to-nearest-even of the fp32 result
+ *   lse      [B, sq, H]       float32, natural log of sum_t exp(scale * q.k_t)
+ *                             over the visible keys; may be NULL (not written)
+ * Supported: D in {64, 128}; R = (H/G)*sq <= 32 query rows per KV head.
+ * A row with no visible key (T_b - sq + s < 0) gets out = 0 and lse = -inf.
+ *
+ * Ownership and ordering: the caller owns every tensor and the stream. All
+ * work is enqueued on `stream` (0 = legacy default stream); no call
+ * synchronises the host except gqa_decode_check_error. Inputs must not be
+ * modified, and outputs not read, until the work on `stream` has completed.
+ *
+ * Errors: functions return GQA_OK (0) or one of the negative codes below and
+ * then enqueue nothing. GQA_ERR_CUDA means a CUDA call failed; the CUDA error
+ * is available from gqa_decode_last_cuda_error(). Device-side faults of the
+ * kind the kernels can detect (a bounded pipeline wait that expired) are
+ * recorded in a per-device status word and reported by
+ * gqa_decode_check_error().
+ */
+#ifndef GQA_DECODE_H
+#define GQA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GQA_OK 0
+#define GQA_ERR_INVALID_ARG -1     /* null pointer, a size <= 0, Tmax < sq, ... */
+#define GQA_ERR_HEAD_RATIO -2      /* H % G != 0 */
+#define GQA_ERR_UNSUPPORTED -3     /* D not in {64,128}, R > 32, sizes out of range */
+#define GQA_ERR_MISALIGNED -4      /* a tensor pointer not 16-byte aligned */
+#define GQA_ERR_WORKSPACE -5       /* caller workspace NULL or smaller than required */
+#define GQA_ERR_CUDA -6            /* a CUDA runtime/driver call failed */
+#define GQA_ERR_DEVICE_TIMEOUT -7  /* a bounded device-side wait expired */
+
+/*
+ * Decode attention for one step, using a workspace the library owns: one
+ * grow-only device buffer per (device, stream), allocated with cudaMalloc on
+ * the first call that needs more than the stream's buffer holds. Calls on the
+ * same stream are ordered; calls on different streams use different buffers.
+ * Make one call per stream before capturing that stream into a CUDA graph, so
+ * that no allocation happens during capture.
+ *
+ * q, k_cache, v_cache, seq_lens, out, lse: device pointers, layouts above.
+ * scale: multiplier applied to q.k (1/sqrt(D) for the pages' definition).
+ * B, sq, H, G, D, Tmax: sizes; stream: the CUDA stream to enqueue on.
+ */
+int gqa_decode(const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* seq_lens, float scale, void* out, float* lse,
+               int B, int sq, int H, int G, int D, int Tmax, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace gqa_decode_ex needs for these sizes on the current
+ * device (the split-KV partial results of section (a7) of the design plus the
+ * per-sequence tile prefix sums). Returns 0 for unsupported arguments.
+ */
+size_t gqa_decode_workspace_bytes(int B, int sq, int H, int G, int D, int Tmax);
+
+/*
+ * Same as gqa_decode, with a caller-owned device workspace of at least
+ * gqa_decode_workspace_bytes(...) bytes, 256-byte aligned. It needs no
+ * initialisation. Two calls that are in flight at the same time must not share
+ * a workspace.
+ */
+int gqa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* seq_lens, float scale, void* out, float* lse,
+                  int B, int sq, int H, int G, int D, int Tmax,
+                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * The work plan a call would use, for inspection and tests. Host-only; needs
+ * no GPU. The KV stream of all (sequence, KV head) units is cut into tiles of
+ * `tile_tokens` tokens; the `ctas` persistent CTAs each take an equal,
+ * contiguous share of the flattened tile list, so a unit's context is split
+ * wherever those shares cut it. `num_sms` is the device's SM count.
+ */
+typedef struct gqa_decode_plan_t {
+    int ctas;              /* grid size of the split-KV kernel */
+    int tile_tokens;       /* tokens per pipeline stage */
+    int row_tiles;         /* 16-row MMA tiles per KV head: ceil(R / 16) */
+    int stages;            /* depth of the shared-memory K/V ring */
+    int threads;           /* threads per CTA (consumer warps + 1 producer warp) */
+    int smem_bytes;        /* dynamic shared memory per CTA */
+    long long max_tiles;   /* B * G * ceil(Tmax / tile_tokens): tiles if every T_b = Tmax */
+} gqa_decode_plan_t;
+
+int gqa_decode_plan(int B, int sq, int H, int G, int D, int Tmax, int num_sms,
+                    gqa_decode_plan_t* plan);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word. Returns GQA_OK, GQA_ERR_DEVICE_TIMEOUT if a kernel gave up on a
+ * bounded wait since the last check (its outputs are then undefined), or
+ * GQA_ERR_CUDA.
+ */
+int gqa_decode_check_error(cudaStream_t stream);
+
+/* The cudaError_t of the last failed CUDA call in this thread (0 if none). */
+int gqa_decode_last_cuda_error(void);
+
+/* A static, human-readable description of a status code. */
+const char* gqa_decode_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_DECODE_H */

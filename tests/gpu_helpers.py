@@ -1,0 +1,106 @@
+"""Shared helpers of the GPU parity tests: move generator output to the device,
+call the CUDA path through the C ABI with guard canaries around the outputs,
+and compare with the oracle within the stated tolerances."""
+from __future__ import annotations
+
+import contextlib
+import os
+
+import numpy as np
+import torch
+
+import grouped_query_decode_gb300 as gq
+import synthetic as syn
+
+# Tolerances of the parity bar: max-abs error on the bf16 output and on the
+# fp32 natural-log LSE.
+OUT_ATOL = 1e-2
+LSE_ATOL = 1e-3
+
+_PAD = 64          # guard elements on each side of an output (keeps 16 B alignment)
+_CANARY_BF16 = 0x7F7F
+_CANARY_F32 = np.float32(-1.2345e29)
+
+
+def to_device_bf16(bits: np.ndarray) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.bfloat16).cuda()
+
+
+def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+@contextlib.contextmanager
+def min_tiles(n):
+    old = os.environ.get("GQA_DECODE_MIN_TILES_PER_CTA")
+    if n is None:
+        os.environ.pop("GQA_DECODE_MIN_TILES_PER_CTA", None)
+    else:
+        os.environ["GQA_DECODE_MIN_TILES_PER_CTA"] = str(n)
+    try:
+        yield
+    finally:
+        if old is None:
+            os.environ.pop("GQA_DECODE_MIN_TILES_PER_CTA", None)
+        else:
+            os.environ["GQA_DECODE_MIN_TILES_PER_CTA"] = old
+
+
+def run_gpu(q, k, v, lens, scale, with_lse=True, device_inputs=None):
+    """Runs gqa_decode on the device. Returns (out float64 [B,sq,H,D], lse
+    float64 [B,sq,H] or None). Checks that the guard words around out and lse
+    are untouched and that no device-side wait expired."""
+    if device_inputs is None:
+        dq, dk, dv = to_device_bf16(q), to_device_bf16(k), to_device_bf16(v)
+        dl = torch.from_numpy(np.ascontiguousarray(lens, dtype=np.int32)).cuda()
+    else:
+        dq, dk, dv, dl = device_inputs
+    B, sq, H, D = dq.shape
+    n = B * sq * H * D
+    out_buf = torch.full((n + 2 * _PAD,), 0, dtype=torch.int16, device="cuda")
+    out_buf.fill_(np.int16(np.uint16(_CANARY_BF16).view(np.int16)))
+    out = out_buf[_PAD:_PAD + n].view(torch.bfloat16).view(B, sq, H, D)
+    lse = None
+    if with_lse:
+        m = B * sq * H
+        lse_buf = torch.full((m + 2 * _PAD,), float(_CANARY_F32), dtype=torch.float32, device="cuda")
+        lse = lse_buf[_PAD:_PAD + m].view(B, sq, H)
+    gq.gqa_decode(dq, dk, dv, dl, scale, out, lse)
+    torch.cuda.synchronize()
+    assert gq.gqa_decode_check_error() == gq.GQA_OK
+    ob = out_buf.cpu().numpy().view(np.uint16)
+    assert np.all(ob[:_PAD] == _CANARY_BF16) and np.all(ob[_PAD + n:] == _CANARY_BF16), "out guard"
+    lse_np = None
+    if with_lse:
+        lb = lse_buf.cpu().numpy()
+        m = B * sq * H
+        assert np.all(lb[:_PAD] == _CANARY_F32) and np.all(lb[_PAD + m:] == _CANARY_F32), "lse guard"
+        lse_np = lb[_PAD:_PAD + m].astype(np.float64).reshape(B, sq, H)
+    return bf16_to_f64(out), lse_np
+
+
+def compare(out, lse, ref_out, ref_lse, rows=None, what=""):
+    """Max-abs bars on out and lse; rows with no visible key must be exactly
+    out = 0 and lse = -inf on both sides."""
+    if rows is not None:
+        out, ref_out = out.reshape(-1, out.shape[-1])[rows], ref_out.reshape(-1, out.shape[-1])[rows]
+        lse, ref_lse = lse.reshape(-1)[rows], ref_lse.reshape(-1)[rows]
+    assert np.all(np.isfinite(out)), f"{what}: non-finite output"
+    err = np.abs(out - ref_out).max() if out.size else 0.0
+    empty = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(lse), empty), f"{what}: -inf lse rows differ"
+    lerr = np.abs(lse[~empty] - ref_lse[~empty]).max() if (~empty).any() else 0.0
+    assert err <= OUT_ATOL, f"{what}: out max-abs error {err:.3e} > {OUT_ATOL}"
+    assert lerr <= LSE_ATOL, f"{what}: lse max-abs error {lerr:.3e} > {LSE_ATOL}"
+    if empty.any():
+        assert np.all(out.reshape(-1, out.shape[-1])[empty.reshape(-1)] == 0), f"{what}: empty rows"
+    return float(err), float(lerr)
+
+
+def make_inputs(B, sq, H, G, D, Tmax, lens, seed, tail=syn.BF16_NAN):
+    lens = np.asarray(lens, dtype=np.int32)
+    q = syn.normal_bf16(seed, syn.STREAM_Q, (B, sq, H, D))
+    k = syn.fill_cache(seed, syn.STREAM_K, B, G, Tmax, D, lens, tail)
+    v = syn.fill_cache(seed, syn.STREAM_V, B, G, Tmax, D, lens, tail)
+    return q, k, v, lens
