@@ -16,12 +16,16 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded device waits: 2 s
 constexpr unsigned kStatusTimeout = 1u;
 
 // Workspace: [int64 prefix[B + 1]] padded to 256 B, then per CTA two partial
-// slots of R*(D + 2) floats: O[R][D] (normalised by its own l), m[R], l[R].
+// slots: O[R][D] (normalised by its own l), m[R], l[R], each slot padded to a
+// multiple of 4 floats so that every slot starts on a 16-byte boundary (the
+// combine kernel reads O with 16-byte loads).
 inline size_t ws_prefix_bytes(int B) {
     size_t b = sizeof(long long) * (size_t)(B + 1);
     return (b + 255) & ~size_t(255);
 }
-inline size_t ws_slot_floats(int R, int D) { return (size_t)R * (D + 2); }
+__host__ __device__ inline size_t ws_slot_floats(int R, int D) {
+    return (size_t)R * D + (((size_t)2 * R + 3) & ~(size_t)3);
+}
 inline size_t ws_total_bytes(int B, int R, int D, int ctas) {
     return ws_prefix_bytes(B) + sizeof(float) * ws_slot_floats(R, D) * 2 * (size_t)ctas;
 }

@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(KernelShape<D, MT>::kThreads, 1)
         } else {
             // Partial: O normalised by its own l, plus m and l, in slot 0 (the
             // CTA's first segment) or 1 (its last).
-            float* slot = p.ws_part + ((size_t)blockIdx.x * 2 + (sg.first ? 0 : 1)) * ((size_t)p.R * (D + 2));
+            float* slot = p.ws_part + ((size_t)blockIdx.x * 2 + (sg.first ? 0 : 1)) * ws_slot_floats(p.R, D);
             float* om = slot + (size_t)p.R * D;
             float* ol = om + p.R;
             if (r_lo < p.R) {
@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(256)
     const long long cl = (ue * P - 1) / W;
     if (cf == cl) return;
 
-    const size_t slot_floats = (size_t)p.R * (D + 2);
+    const size_t slot_floats = ws_slot_floats(p.R, D);
     for (int i = threadIdx.x; i < total; i += blockDim.x) {
         const int r = i / C4, c = (i % C4) * 4;
         float M = -INFINITY;

@@ -175,3 +175,19 @@ def test_argument_errors_on_gpu():
     with pytest.raises(TypeError):
         gq.gqa_decode(dq.float(), dk, dv, dl, 0.1, out, None)
     assert gq.gqa_decode_check_error() == gq.GQA_OK
+
+
+@pytest.mark.parametrize("H,G,sq", [(4, 2, 1), (6, 2, 1), (10, 2, 1), (6, 1, 1), (7, 1, 1),
+                                    (24, 1, 1), (31, 1, 1), (5, 1, 5), (3, 1, 9)],
+                         ids=lambda x: str(x))
+def test_every_row_count(H, G, sq):
+    """Row counts R = (H/G)*sq that are not multiples of anything: partial
+    slots, padded MMA rows and the combine's addressing for each."""
+    lens = [1, 70, 129, 300]
+    B, Tmax, D = len(lens), 320, 128
+    q, k, v, lens = make_inputs(B, sq, H, G, D, Tmax, lens, seed=400 + H * 7 + G + sq)
+    ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, 0.1, threads=8)
+    for mt in (1, 3):
+        with min_tiles(mt):
+            out, lse = run_gpu(q, k, v, lens, 0.1)
+        compare(out, lse, ref_out, ref_lse, what=f"R={H // G * sq}")
