@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Decode-attention benchmark: µs per decode step and achieved HBM GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step is one gqa_decode call (split-KV kernel + LSE combine) over the whole
+workload: every sequence, every query head, one layer. The default workload is
+the Llama-3-8B-shaped layer (B=16, H=32, G=8, D=128, T=4096). Inputs are seeded
+synthetic N(0,1) bf16 tensors from the synthetic/ generator.
+
+value    = algorithmic bytes per step / device time per step (GB/s, all ranks)
+e2e      = the same with the step's inputs copied from pinned host memory and its
+           outputs copied back inside the timed region
+roofline = the per-call duration measured with CUDA events on the launching
+           stream against the measured HBM copy bandwidth
+cpu_baseline = the fp64 CPU oracle (test infrastructure) on the host cores
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+on its own GPU (the path has no exchange step); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic as syn  # noqa: E402
+
+METRIC = "decode-attention µs/step and achieved HBM GB/s (% of GB300 peak) at 1 GPU"
+DEFAULT_WORKLOAD = "llama3_8b_layer"
+PROFILES = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = [os.path.join(ROOT, "grouped_query_decode_gb300", "csrc", f) for f in
+                  ("gqa_splitkv.cuh", "gqa_common.h", "ptx.cuh", "gqa_launch_impl.cuh", "api.cu")]
+
+
+# ------------------------------------------------------------ accounting
+
+def kv_bytes(G: int, D: int, lens, elem_bytes: int = 2) -> int:
+    """K and V bytes one decode step must read: 2 (K and V) x sum_b T_b x G x D
+    x element size -- the KV-cache sizing formula of "GQA analysis" (section
+    "KV cache") for one layer, summed over the batch's actual lengths."""
+    return 2 * int(np.sum(np.asarray(lens, dtype=np.int64))) * G * D * elem_bytes
+
+
+def algorithmic_bytes(B: int, sq: int, H: int, G: int, D: int, lens) -> int:
+    """Bytes a step must move at minimum: the valid K/V, Q in, O out (bf16),
+    LSE out (fp32) and the lengths (int32). Tmax padding is not counted."""
+    return kv_bytes(G, D, lens) + 2 * (B * sq * H * D * 2) + B * sq * H * 4 + 4 * B
+
+
+def algorithmic_flops(sq: int, H: int, D: int, lens) -> int:
+    """QK^T and PV multiply-adds: each query row does T_b*D of each ("keep query
+    heads, cut KV heads", section "what shrinks and what does not": the score
+    and weighted-sum counts carry no G), 2 flops per multiply-add."""
+    return 4 * sq * H * D * int(np.sum(np.asarray(lens, dtype=np.int64)))
+
+
+# --------------------------------------------------------------- helpers
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _source_digest() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(workload: str):
+    """DRAM bytes per launch of the split-KV kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    path = os.path.join(PROFILES, f"ncu_splitkv_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_sources_sha256_16") != _source_digest():
+        return None
+    try:
+        return int(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while work runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------- CPU oracle
+
+def time_oracle(cfg, q, k, v, lens, budget_s: float, max_reps: int | None = None):
+    """Times the oracle (as it stands) over the whole step's rows, split over
+    the host's cores; repeats the step until about budget_s of wall time."""
+    import oracle
+    threads = os.cpu_count() or 1
+    orc = oracle.get()
+    times = []
+    t_all = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        orc.gqa_decode(q, k, v, lens, cfg.scale, threads=threads)
+        times.append(time.perf_counter() - t0)
+        if max_reps is not None and len(times) >= max_reps:
+            break
+        if max_reps is None and time.perf_counter() - t_all >= budget_s:
+            break
+    return times, threads
+
+
+def run_reference(args, cfg):
+    """The reference arm: the fp64 CPU oracle, the only other implementation of
+    this path there is, timed on the host cores over whole decode steps."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    q, k, v, lens = syn.make_inputs(cfg, tail_bits=syn.BF16_ZERO)
+    nbytes = algorithmic_bytes(cfg.B, cfg.sq, cfg.H, cfg.G, cfg.D, lens)
+    time_oracle(cfg, q, k, v, lens, 0, max_reps=max(1, args.warmup))
+    times, threads = time_oracle(cfg, q, k, v, lens, 0, max_reps=args.steps)
+    t = sum(times) / len(times)
+    value = nbytes / t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config_dict(cfg, lens, l2_note="host memory"),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"whole decode step ({cfg.B * cfg.sq * cfg.H} query rows), "
+                                   f"{args.steps} steps"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config_dict(cfg, lens, l2_note):
+    return {"workload": cfg.name, "B": cfg.B, "sq": cfg.sq, "H": cfg.H, "G": cfg.G, "D": cfg.D,
+            "Tmax": cfg.Tmax, "sum_T": int(np.sum(lens)), "scale": cfg.scale, "seed": cfg.seed,
+            "inputs": "Q,K,V i.i.d. N(0,1) rounded to bf16", "l2": l2_note}
+
+
+# ------------------------------------------------------------ GPU arm
+
+def run_gpu(args, cfg):
+    import torch
+    import torch.distributed as dist
+
+    import grouped_query_decode_gb300 as gq
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    q, k, v, lens = syn.make_inputs(cfg, tail_bits=syn.BF16_ZERO)
+    nbytes = algorithmic_bytes(cfg.B, cfg.sq, cfg.H, cfg.G, cfg.D, lens)
+    flops = algorithmic_flops(cfg.sq, cfg.H, cfg.D, lens)
+
+    def to_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    cache_bytes = 2 * k.nbytes
+    copies = max(2, math.ceil(4 * l2 / cache_bytes))
+    dq = to_dev(q)
+    dl = torch.from_numpy(lens).to(dev)
+    dks = [to_dev(k) for _ in range(copies)]
+    dvs = [to_dev(v) for _ in range(copies)]
+    out = torch.empty(cfg.B, cfg.sq, cfg.H, cfg.D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(cfg.B, cfg.sq, cfg.H, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        c = i % copies
+        gq.gqa_decode(dq, dks[c], dvs[c], dl, cfg.scale, out, lse, stream=stream)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    assert gq.gqa_decode_check_error(stream) == gq.GQA_OK
+
+    # Timed region: exactly K steps, bracketed by barrier + synchronize.
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.15)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    ms_total = e0.elapsed_time(e1)
+    # keep sampling the same work a little longer if the region was short
+    t_tail = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t_tail < max(0.0, 0.6 - t_wall):
+        step(i)
+        i += 1
+        if i % 256 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    sampler.stop()
+    clocks = sampler.summary()
+    clocks["window"] = "timed region" if t_wall >= 0.6 else "timed region + untimed tail of the same step"
+
+    ms_step = ms_total / args.steps
+    if ws > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = ws * nbytes / (ms_step * 1e-3) / 1e9
+
+    # Per-call durations (events around each call, same stream) for the roofline.
+    n_calls = min(args.steps, 200) if args.steps > 0 else 0
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_calls)]
+    for i, (a, b) in enumerate(evs):
+        a.record(stream)
+        step(i)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    call_ms = [a.elapsed_time(b) for a, b in evs]
+    call_ms_mean = statistics.mean(call_ms) if call_ms else float("nan")
+    peak, peak_kind = _peaks()
+    achieved = nbytes / (call_ms_mean * 1e-3) / 1e9
+    assert gq.gqa_decode_check_error(stream) == gq.GQA_OK
+
+    # End to end: inputs from pinned host memory, outputs back, every step.
+    hq = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hk = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hv = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hl = torch.from_numpy(lens).pin_memory()
+    ho = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dks[0].copy_(hk, non_blocking=True)
+        dvs[0].copy_(hv, non_blocking=True)
+        dl.copy_(hl, non_blocking=True)
+        gq.gqa_decode(dq, dks[0], dvs[0], dl, cfg.scale, out, lse, stream=stream)
+        ho.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = hq.nbytes + hk.nbytes + hv.nbytes + hl.nbytes
+    d2h = ho.nbytes + hlse.nbytes
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if ws == 1 and not args.no_cpu_baseline:
+            times, threads = time_oracle(cfg, q, k, v, lens, args.cpu_budget_s)
+            tc = statistics.median(times)
+            cpu = {"value": nbytes / tc / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                   "sample": f"whole decode step ({cfg.B * cfg.sq * cfg.H} query rows) x "
+                             f"{len(times)} repetitions, median"}
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "us_per_step": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": _config_dict(cfg, lens, l2_note=f"inputs larger than L2: {copies} rotating "
+                                                       f"K/V copies of {cache_bytes >> 20} MiB vs "
+                                                       f"{l2 >> 20} MiB L2"),
+            "query_tokens_per_s": ws * cfg.B * cfg.sq / (ms_step * 1e-3),
+            "tflops": ws * flops / (ms_step * 1e-3) / 1e12,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": _ncu_traffic(cfg.name),
+                         "peak_kind": peak_kind,
+                         "kernel": "gqa_splitkv_kernel (+ PDL-overlapped gqa_combine_kernel)",
+                         "duration": "mean per-call CUDA-event time over "
+                                     f"{n_calls} calls, {call_ms_mean * 1e3:.2f} us",
+                         "algorithmic_bytes_per_launch": nbytes},
+            "cpu_baseline": cpu,
+            "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9 * ws, "unit": "GB/s",
+                    "us_per_step": e2e_ms * 1e3,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=[c.name for c in syn.CONFIGS])
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    cfg = syn.config_by_name(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_gpu(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

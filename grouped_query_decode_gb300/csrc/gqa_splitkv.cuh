@@ -551,18 +551,22 @@ __global__ void __launch_bounds__(256)
     const size_t slot_floats = ws_slot_floats(p.R, D);
     for (int i = threadIdx.x; i < total; i += blockDim.x) {
         const int r = i / C4, c = (i % C4) * 4;
+        // CTAs cf..cl cover the unit; when there are fewer tiles than CTAs some
+        // of them have an empty share and wrote no partial.
         float M = -INFINITY;
         for (long long cta = cf; cta <= cl; ++cta) {
-            const int slot = (cta * W / P >= ub) ? 0 : 1;
-            const float* part = p.ws_part + ((size_t)cta * 2 + slot) * slot_floats;
+            const long long clo = cta * W / P, chi = (cta + 1) * W / P;
+            if (clo >= chi) continue;
+            const float* part = p.ws_part + ((size_t)cta * 2 + (clo >= ub ? 0 : 1)) * slot_floats;
             M = fmaxf(M, part[(size_t)p.R * D + r]);
         }
         float L = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (M != -INFINITY) {
             for (long long cta = cf; cta <= cl; ++cta) {
-                const int slot = (cta * W / P >= ub) ? 0 : 1;
-                const float* part = p.ws_part + ((size_t)cta * 2 + slot) * slot_floats;
+                const long long clo = cta * W / P, chi = (cta + 1) * W / P;
+                if (clo >= chi) continue;
+                const float* part = p.ws_part + ((size_t)cta * 2 + (clo >= ub ? 0 : 1)) * slot_floats;
                 const float m = part[(size_t)p.R * D + r];
                 const float l = part[(size_t)p.R * D + p.R + r];
                 if (m == -INFINITY || l == 0.f) continue;
