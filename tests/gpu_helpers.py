@@ -12,9 +12,14 @@ import torch
 import grouped_query_decode_gb300 as gq
 import synthetic as syn
 
-# Tolerances of the parity bar: max-abs error on the bf16 output and on the
-# fp32 natural-log LSE.
+# Tolerances of the parity bar: max-abs error 1e-2 on the bf16 output and 1e-3
+# on the fp32 natural-log LSE. The output bar adds bf16's own rounding: the
+# format keeps 8 significant bits, so rounding alone moves a value by up to
+# 2^-8 |x| (1/64 for |x| in [4, 8), which short sequences with a sharp softmax
+# reach). On the decode workloads |out| stays below ~0.1 and the bar is
+# 1e-2 + <4e-4.
 OUT_ATOL = 1e-2
+OUT_RTOL_BF16 = 2.0 ** -8
 LSE_ATOL = 1e-3
 
 _PAD = 64          # guard elements on each side of an output (keeps 16 B alignment)
@@ -87,11 +92,15 @@ def compare(out, lse, ref_out, ref_lse, rows=None, what=""):
         out, ref_out = out.reshape(-1, out.shape[-1])[rows], ref_out.reshape(-1, out.shape[-1])[rows]
         lse, ref_lse = lse.reshape(-1)[rows], ref_lse.reshape(-1)[rows]
     assert np.all(np.isfinite(out)), f"{what}: non-finite output"
-    err = np.abs(out - ref_out).max() if out.size else 0.0
+    diff = np.abs(out - ref_out)
+    excess = diff - (OUT_ATOL + OUT_RTOL_BF16 * np.abs(ref_out))
+    err = diff.max() if out.size else 0.0
     empty = np.isneginf(ref_lse)
     assert np.array_equal(np.isneginf(lse), empty), f"{what}: -inf lse rows differ"
     lerr = np.abs(lse[~empty] - ref_lse[~empty]).max() if (~empty).any() else 0.0
-    assert err <= OUT_ATOL, f"{what}: out max-abs error {err:.3e} > {OUT_ATOL}"
+    assert (excess <= 0).all(), (f"{what}: out error {diff.flat[excess.argmax()]:.3e} at "
+                                 f"|ref| {np.abs(ref_out).flat[excess.argmax()]:.3e} above "
+                                 f"{OUT_ATOL} + 2^-8 |ref|")
     assert lerr <= LSE_ATOL, f"{what}: lse max-abs error {lerr:.3e} > {LSE_ATOL}"
     if empty.any():
         assert np.all(out.reshape(-1, out.shape[-1])[empty.reshape(-1)] == 0), f"{what}: empty rows"
