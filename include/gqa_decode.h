@@ -86,8 +86,9 @@ int gqa_decode(const void* q, const void* k_cache, const void* v_cache,
 
 /*
  * Bytes of device workspace gqa_decode_ex needs for these sizes on the current
- * device (the split-KV partial results of section (a7) of the design plus the
- * per-sequence tile prefix sums). Returns 0 for unsupported arguments.
+ * device: two partial-result slots (O[R][D], running max m[R], sum l[R]) per
+ * split-KV CTA plus the per-sequence tile prefix sums. Returns 0 for
+ * unsupported arguments.
  */
 size_t gqa_decode_workspace_bytes(int B, int sq, int H, int G, int D, int Tmax);
 
