@@ -62,6 +62,8 @@ def load():
             lib.gqa_decode.restype = i32
             lib.gqa_decode_ex.argtypes = [vp, vp, vp, vp, f32, vp, vp, *shape, vp, sz, vp]
             lib.gqa_decode_ex.restype = i32
+            lib.gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, f32, vp, vp, *shape, vp]
+            lib.gqa_decode_noalloc.restype = i32
             lib.gqa_decode_workspace_bytes.argtypes = shape
             lib.gqa_decode_workspace_bytes.restype = sz
             lib.gqa_decode_plan.argtypes = [*shape, i32, ctypes.POINTER(PlanT)]
@@ -143,6 +145,25 @@ def gqa_decode_ex(q, k_cache, v_cache, seq_lens, scale, out, lse, workspace, str
                               _stream_handle(stream, q.device))
     if rc != GQA_OK:
         raise GQADecodeError(rc, "gqa_decode_ex")
+
+
+# Size of the fixed per-device scratch array gqa_decode_noalloc draws from.
+GQA_NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def gqa_decode_noalloc(q, k_cache, v_cache, seq_lens, scale, out, lse=None, stream=None):
+    """One decode step that allocates no device memory: the scratch comes from
+    a fixed 8 MiB array the library keeps on each GPU. For callers that may not
+    allocate once running (a pre-reserved memory pool, a framework plugin with
+    no allocator, a loop that cannot take cudaMalloc's synchronisation). Calls
+    on one device share that array, so calls that overlap on the GPU race."""
+    B, sq, H, G, D, Tmax = _shapes(q, k_cache, v_cache, seq_lens, out, lse)
+    rc = load().gqa_decode_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                   seq_lens.data_ptr(), float(scale), out.data_ptr(),
+                                   None if lse is None else lse.data_ptr(), B, sq, H, G, D, Tmax,
+                                   _stream_handle(stream, q.device))
+    if rc != GQA_OK:
+        raise GQADecodeError(rc, "gqa_decode_noalloc")
 
 
 def gqa_decode_workspace_bytes(B, sq, H, G, D, Tmax) -> int:

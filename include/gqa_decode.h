@@ -131,6 +131,34 @@ int gqa_decode_plan(int B, int sq, int H, int G, int D, int Tmax, int num_sms,
  */
 int gqa_decode_check_error(cudaStream_t stream);
 
+/*
+ * Allocation-free variant of gqa_decode, for callers that must not allocate
+ * device memory while they run: a serving engine that hands all device memory
+ * to its own pool at start-up, a plugin inside another framework that gets
+ * tensors but no allocator, or a decode loop that cannot afford cudaMalloc's
+ * implicit synchronisation. The pages have no counterpart of this; it is a
+ * property of this library's interface, not of the attention it computes.
+ *
+ * Same arguments, layouts and results as gqa_decode. The split-KV scratch
+ * comes from a fixed array of GQA_NOALLOC_SCRATCH_BYTES in device memory that
+ * every GPU which loads the library holds until the process exits; the call
+ * makes no cudaMalloc or cudaFree. The first call on a device looks up that
+ * array's device address (with the device current), so make that first call
+ * before capturing a stream into a CUDA graph.
+ *
+ * The array is shared by every call on a device and keeps the last call's
+ * contents: two calls that overlap on the GPU (different streams, no ordering
+ * between them) race on it and give undefined results; order them, or use
+ * gqa_decode_ex with one workspace each. A problem whose scratch need,
+ * gqa_decode_workspace_bytes(...), exceeds GQA_NOALLOC_SCRATCH_BYTES is
+ * rejected with GQA_ERR_WORKSPACE and nothing is enqueued.
+ */
+#define GQA_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB per device */
+
+int gqa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* seq_lens, float scale, void* out, float* lse,
+                       int B, int sq, int H, int G, int D, int Tmax, cudaStream_t stream);
+
 /* The cudaError_t of the last failed CUDA call in this thread (0 if none). */
 int gqa_decode_last_cuda_error(void);
 
