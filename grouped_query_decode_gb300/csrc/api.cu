@@ -5,6 +5,10 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <unistd.h>
+
+#include <atomic>
+#include <chrono>
 #include <cstdint>
 #include <cstdlib>
 #include <map>
@@ -111,6 +115,38 @@ int min_tiles_per_cta() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A 48-bit tag per call for the workspace's arrival counters. It starts from
+// the clock and the process id so that a workspace left over from another
+// process or an aborted call is unlikely to hold a matching tag.
+unsigned long long next_epoch() {
+    static std::atomic<unsigned long long> counter{
+        (static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count()) *
+             0x9E3779B97F4A7C15ull ^
+         (static_cast<unsigned long long>(getpid()) << 20))};
+    const unsigned long long e = counter.fetch_add(1) & 0xFFFFFFFFFFFFull;
+    return e;
+}
+
+// Test hooks, read per call from the environment: GQA_DECODE_DEBUG_TIMEOUT_MS
+// shortens the limit of every device-side wait (default 2 s), and
+// GQA_DECODE_DEBUG_SKIP_TILE=n makes CTA 0 skip loading its n-th K/V tile, so
+// that its consumers' bounded wait expires and the call reports
+// GQA_ERR_DEVICE_TIMEOUT -- the failure path, exercised without faulting.
+void debug_knobs(unsigned long long* timeout_ns, int* skip_tile) {
+    const char* t = std::getenv("GQA_DECODE_DEBUG_TIMEOUT_MS");
+    const long long ms = t ? std::atoll(t) : 0;
+    *timeout_ns = ms > 0 ? (unsigned long long)ms * 1000000ull : kWaitTimeoutNs;
+    const char* k = std::getenv("GQA_DECODE_DEBUG_SKIP_TILE");
+    *skip_tile = k ? std::atoi(k) : -1;
+}
+
+// Grid size override for sweeps of the plan (unset: the heuristic decides).
+int forced_ctas() {
+    const char* s = std::getenv("GQA_DECODE_CTAS");
+    const int x = s ? std::atoi(s) : 0;
+    return x > 0 ? x : 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -126,6 +162,8 @@ int gqa_decode_plan(int B, int sq, int H, int G, int D, int Tmax, int num_sms,
     const long long max_tiles = (long long)B * G * tiles_per_unit;
     long long ctas = (max_tiles + min_tiles_per_cta() - 1) / min_tiles_per_cta();
     if (ctas > num_sms) ctas = num_sms;
+    if (forced_ctas() > 0) ctas = forced_ctas();
+    if (ctas > kMaxMergeContrib) ctas = kMaxMergeContrib;
     if (ctas < 1) ctas = 1;
     plan->ctas = (int)ctas;
     plan->tile_tokens = kTileTokens;
@@ -142,7 +180,7 @@ size_t gqa_decode_workspace_bytes(int B, int sq, int H, int G, int D, int Tmax) 
     if (device_info(&info) != GQA_OK) return 0;
     gqa_decode_plan_t plan;
     if (gqa_decode_plan(B, sq, H, G, D, Tmax, info.sms, &plan) != GQA_OK) return 0;
-    return ws_total_bytes(B, (H / G) * sq, D, plan.ctas);
+    return ws_total_bytes(B, G, (H / G) * sq, D, plan.ctas);
 }
 
 int gqa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
@@ -162,7 +200,7 @@ int gqa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
     st = gqa_decode_plan(B, sq, H, G, D, Tmax, info.sms, &plan);
     if (st != GQA_OK) return st;
     const int R = (H / G) * sq;
-    const size_t need = ws_total_bytes(B, R, D, plan.ctas);
+    const size_t need = ws_total_bytes(B, G, R, D, plan.ctas);
     if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return GQA_ERR_WORKSPACE;
 
@@ -175,8 +213,9 @@ int gqa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
     a.p.seq_lens = seq_lens;
     a.p.out = static_cast<uint16_t*>(out);
     a.p.lse = lse;
-    a.p.ws_prefix = static_cast<long long*>(workspace);
-    a.p.ws_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws_prefix_bytes(B));
+    a.p.ws_counters = static_cast<unsigned long long*>(workspace);
+    a.p.ws_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws_counter_bytes(B, G));
+    a.p.epoch = next_epoch();
     a.p.status = info.status;
     a.p.scale_log2 = scale * 1.4426950408889634f;
     a.p.B = B;
@@ -187,6 +226,8 @@ int gqa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
     a.p.R = R;
     a.p.heads_per_group = H / G;
     a.p.ctas = plan.ctas;
+    a.p.even_rule = forced_ctas() > 0 ? 0 : 1;
+    debug_knobs(&a.p.wait_timeout_ns, &a.p.skip_tile);
     a.row_tiles = plan.row_tiles;
     a.pdl = true;
     a.stream = stream;

@@ -10,24 +10,30 @@ constexpr int kTileTokens = 64;   // tokens per pipeline stage (one TMA box of r
 constexpr int kSlices = 4;        // consumer warps per 16-row tile, 16 tokens each per stage
 constexpr int kMaxRowTiles = 2;   // R <= 32 query rows per KV head
 constexpr int kBoxCols = 64;      // bf16 elements per 128-byte swizzle box row
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded device waits: 2 s
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded device waits: 2 s by default
+constexpr float kRescaleSlack = 8.0f;   // lazy online-softmax rescale threshold (base 2)
+// Most CTAs whose partials one merge can combine (the merge keeps per-
+// contributor state in shared memory); the grid never exceeds it.
+constexpr int kMaxMergeContrib = 180;
 
 // Status bits of the per-device status word.
 constexpr unsigned kStatusTimeout = 1u;
 
-// Workspace: [int64 prefix[B + 1]] padded to 256 B, then per CTA two partial
-// slots: O[R][D] (normalised by its own l), m[R], l[R], each slot padded to a
-// multiple of 4 floats so that every slot starts on a 16-byte boundary (the
-// combine kernel reads O with 16-byte loads).
-inline size_t ws_prefix_bytes(int B) {
-    size_t b = sizeof(long long) * (size_t)(B + 1);
+// Workspace: one 64-bit arrival counter per (sequence, KV head, 16-row tile),
+// padded to 256 B, then per CTA two partial slots: O[R][D] (normalised by its
+// own l), m[R], l[R], each slot padded to a multiple of 4 floats so that every
+// slot starts on a 16-byte boundary (the merge reads O with 16-byte loads).
+// The counters carry the call's epoch, so no part of the workspace needs
+// clearing.
+inline size_t ws_counter_bytes(int B, int G) {
+    size_t b = sizeof(unsigned long long) * (size_t)B * G * kMaxRowTiles;
     return (b + 255) & ~size_t(255);
 }
 __host__ __device__ inline size_t ws_slot_floats(int R, int D) {
     return (size_t)R * D + (((size_t)2 * R + 3) & ~(size_t)3);
 }
-inline size_t ws_total_bytes(int B, int R, int D, int ctas) {
-    return ws_prefix_bytes(B) + sizeof(float) * ws_slot_floats(R, D) * 2 * (size_t)ctas;
+inline size_t ws_total_bytes(int B, int G, int R, int D, int ctas) {
+    return ws_counter_bytes(B, G) + sizeof(float) * ws_slot_floats(R, D) * 2 * (size_t)ctas;
 }
 
 struct DecodeParams {
@@ -35,27 +41,51 @@ struct DecodeParams {
     const int32_t* seq_lens; // [B]
     uint16_t* out;           // [B, sq, H, D] bf16 bits
     float* lse;              // [B, sq, H] or nullptr
-    long long* ws_prefix;    // [B + 1]
-    float* ws_part;          // [ctas][2][R*(D+2)]
+    unsigned long long* ws_counters;  // [B*G][kMaxRowTiles] arrival counters
+    float* ws_part;          // [ctas][2][slot]
+    unsigned long long epoch;  // this call's tag in the counters (48 bits)
     unsigned* status;        // per-device status word (kStatus* bits)
+    unsigned long long wait_timeout_ns;  // limit of every device-side wait
     float scale_log2;        // scale * log2(e)
     int B, sq, H, G, Tmax, R, heads_per_group, ctas;
+    int even_rule;           // 1: use fewer CTAs when that splits no unit (see kernel)
+    int skip_tile;           // fault injection for tests: CTA 0 never loads its tile
+                             // number skip_tile (-1: off), so its consumers' wait expires
 };
 
+// One CTA per SM. Every 16-row tile of the group has four consumer warps
+// ("slices") that take 16 of a stage's 64 tokens each; one more warp issues
+// the TMA copies. With two row tiles (9 warps, which the register file
+// allocates as 12) a thread gets 168 registers, so those warps keep their Q
+// fragments in shared memory rather than in registers.
 template <int D, int MT>
 struct KernelShape {
     static constexpr int kConsumerWarps = kSlices * MT;
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+    // Registers per thread: the 64K register file for one CTA, with warps
+    // counted in the allocation steps of 4, in steps of 8 registers, <= 255.
+    static constexpr int kAllocWarps = (kThreads / 32 + 3) / 4 * 4;
+    static constexpr int kMaxRegs =
+        (65536 / (kAllocWarps * 32)) / 8 * 8 > 255 ? 255 : (65536 / (kAllocWarps * 32)) / 8 * 8;
+    static constexpr bool kQInSmem = MT > 1;
+    static constexpr int kQBytesPerWarp = kQInSmem ? 16 * D * 2 : 0;
     static constexpr int kBoxes = D / kBoxCols;
     static constexpr int kTileBytes = kTileTokens * D * 2;   // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kMergeBytes = MT * (kSlices - 1) * 16 * D * 4;
+    // Per row tile: the slice-merge buffer (3 slices x 16 x D floats), which
+    // the cross-CTA merge reuses for a slot index, 16 maxima and 16 weights per
+    // contributor.
+    static constexpr int kMergeFloatsPerTile =
+        (kSlices - 1) * 16 * D > kMaxMergeContrib * 33 ? (kSlices - 1) * 16 * D
+                                                         : kMaxMergeContrib * 33;
+    static constexpr int kMergeBytes = MT * kMergeFloatsPerTile * 4;
     static constexpr int kMlBytes = MT * kSlices * 16 * 2 * 4;
+    static constexpr int kQBytes = kConsumerWarps * kQBytesPerWarp;
     static constexpr int kStages = D == 128 ? (MT == 1 ? 5 : 4) : 8;
-    static constexpr int kBarBytes = 8 * (2 * kStages + 2 * MT) + 64;
+    static constexpr int kBarBytes = 8 * (2 * kStages + 4 * MT) + 64;
     // +1024 so the ring can be aligned to the 1 KB swizzle atom at run time.
     static constexpr int kSmemBytes =
-        1024 + kStages * kStageBytes + kMergeBytes + kMlBytes + kBarBytes;
+        1024 + kStages * kStageBytes + kMergeBytes + kMlBytes + kQBytes + kBarBytes;
 };
 
 }  // namespace gqa

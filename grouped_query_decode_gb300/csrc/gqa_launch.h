@@ -18,7 +18,7 @@ struct LaunchArgs {
     cudaStream_t stream;
 };
 
-// Enqueue the split-KV kernel and the combine kernel for D = 64 / D = 128.
+// Enqueue the split-KV kernel (one launch per decode step) for D = 64 / D = 128.
 cudaError_t launch_d64(const LaunchArgs& a);
 cudaError_t launch_d128(const LaunchArgs& a);
 

@@ -9,7 +9,7 @@
 namespace gqa {
 
 template <int D, int MT>
-cudaError_t launch_splitkv_and_combine(const LaunchArgs& a) {
+cudaError_t launch_splitkv(const LaunchArgs& a) {
     using KS = KernelShape<D, MT>;
     // The shared-memory opt-in is per function and per device.
     static std::atomic<unsigned long long> attr_set_mask{0};
@@ -34,17 +34,7 @@ cudaError_t launch_splitkv_and_combine(const LaunchArgs& a) {
     cfg.stream = a.stream;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, gqa_splitkv_kernel<D, MT>, a.tm_k, a.tm_v, a.p);
-    if (e != cudaSuccess) return e;
-
-    cudaLaunchConfig_t cc = {};
-    cc.gridDim = dim3(a.p.B * a.p.G);
-    cc.blockDim = dim3(256);
-    cc.dynamicSmemBytes = 0;
-    cc.stream = a.stream;
-    cc.attrs = attr;
-    cc.numAttrs = a.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cc, gqa_combine_kernel<D>, a.p);
+    return cudaLaunchKernelEx(&cfg, gqa_splitkv_kernel<D, MT>, a.tm_k, a.tm_v, a.p);
 }
 
 }  // namespace gqa

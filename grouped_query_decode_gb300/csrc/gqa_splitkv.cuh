@@ -5,20 +5,22 @@
 // (b-major, then g, then position) and each CTA takes an equal contiguous
 // share of that list. A CTA therefore walks one or more "segments" (runs of
 // tiles of one unit). A segment that covers a whole unit is finished in the
-// CTA and written straight to out/lse; a segment that covers part of a unit
-// leaves a partial (O, m, l) that the combine kernel merges.
+// CTA and written straight to out/lse. A segment that covers part of a unit
+// leaves a partial (O, m, l) in the workspace and counts itself on the unit's
+// arrival counter; the CTA that arrives last merges the unit's partials with
+// the log-sum-exp rescale and writes out/lse. One launch does the whole step.
 //
-// Inside a CTA a producer warp streams K and V tiles HBM -> shared memory
-// with TMA tensor copies (128-byte swizzle, so the ldmatrix reads below are
+// Inside a CTA one thread streams K and V tiles HBM -> shared memory with TMA
+// tensor copies (128-byte swizzle, so the ldmatrix reads below are
 // bank-conflict free) into a ring of mbarrier-guarded stages. All R = (H/G)*sq
 // query rows of the unit's group sit in registers as the A operand of
-// m16n8k16 bf16 tensor-core MMAs (one 16-row tile per consumer warp group),
-// so each K/V byte is read from HBM once for the whole group -- "GQA
-// analysis", section "Grouped broadcast": the group index selects the KV head,
-// K/V are never copied per query head. Four consumer warps per row tile split
-// each 64-token stage 16 tokens apiece, run an online softmax in fp32 (base 2,
-// running max and sum per row, quad shuffles), and merge their states through
-// shared memory at the end of each segment.
+// m16n8k16 bf16 tensor-core MMAs (one 16-row tile per group of four consumer
+// warps), so each K/V byte is read from HBM once for the whole group -- "GQA
+// analysis", section "Grouped broadcast": the group index selects the KV head
+// and K/V are never copied per query head. The four consumer warps of a row
+// tile split each 64-token stage 16 tokens apiece, run an online softmax in
+// fp32 (base 2, running max and sum per row, quad shuffles), and merge their
+// states through shared memory at the end of each segment.
 #pragma once
 
 #include <cstdint>
@@ -32,11 +34,14 @@ struct Segment {
     int b, g, tb;        // unit and its valid length (clamped)
     int t0;              // first tile of the segment within the unit
     int ntiles;          // tiles in the segment
+    long long ub, ue;    // the unit's tile range in the flattened list
     bool complete;       // the segment covers the whole unit
     bool first;          // the CTA's first segment (partial slot 0, else slot 1)
 };
 
 __device__ __forceinline__ int clamp_len(int t, int Tmax) { return t < 0 ? 0 : (t > Tmax ? Tmax : t); }
+
+__device__ __forceinline__ long long tiles_of(int tb) { return (tb + kTileTokens - 1) / kTileTokens; }
 
 // Walks the CTA's share [lo, hi) of the flattened tile list, one segment at a
 // time. Every warp runs its own copy; they all see the same sequence.
@@ -49,7 +54,7 @@ struct SegmentWalker {
     __device__ bool next(Segment& s) {
         while (x < hi) {
             const int tb = clamp_len(__ldg(seq_lens + b), Tmax);
-            const long long nt = (tb + kTileTokens - 1) / kTileTokens;
+            const long long nt = tiles_of(tb);
             const long long span = nt * G;
             if (x >= pre_b + span) {
                 pre_b += span;
@@ -65,6 +70,8 @@ struct SegmentWalker {
             s.tb = tb;
             s.t0 = (int)(x - ub);
             s.ntiles = (int)(e - x);
+            s.ub = ub;
+            s.ue = ue;
             s.complete = (x == ub) && (e == ue);
             s.first = (x == lo);
             x = e;
@@ -77,13 +84,13 @@ struct SegmentWalker {
 // Bounded wait on an mbarrier phase. On expiry, or when another warp of the
 // CTA has already given up, it records the failure and returns false.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                           unsigned* status) {
+                                           unsigned* status, uint64_t timeout_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        if (global_timer_ns() - t0 > timeout_ns) {
             *abort_flag = 1;
             atomicOr(status, kStatusTimeout);
             return false;
@@ -91,15 +98,108 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     }
 }
 
+// Counts one arrival on a unit's counter and returns the arrivals so far in
+// this call. The counter holds (epoch << 16) | count; the first arrival of a
+// call finds another epoch there and restarts the count, so the workspace
+// never needs clearing. A CAS only fails when another CTA's CAS succeeded, so
+// the loop ends; it is bounded all the same.
+__device__ __forceinline__ unsigned arrive_unit(unsigned long long* ctr, unsigned long long epoch,
+                                                unsigned* status) {
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr);
+    for (int i = 0; i < (1 << 20); ++i) {
+        const unsigned long long next = ((old >> 16) == epoch) ? old + 1 : ((epoch << 16) | 1ull);
+        const unsigned long long prev = atomicCAS(ctr, old, next);
+        if (prev == old) return (unsigned)(next & 0xffffu);
+        old = prev;
+    }
+    atomicOr(status, kStatusTimeout);
+    return 0;
+}
+
+// The CTA holding tile x, and CTA c's share, for the equal partition of W
+// tiles over P CTAs.
+__device__ __forceinline__ long long cta_of_tile(long long x, long long W, long long P) {
+    return ((x + 1) * P - 1) / W;
+}
+
+// Hands out the CTA's tiles in order and issues their TMA copies into the
+// ring: stage it % S, armed on full[it % S] once empty[it % S] shows that the
+// consumers are done with the tile S places earlier.
+template <int D, int S>
+struct TileIssuer {
+    SegmentWalker walk;
+    Segment sg;
+    int i = 0;
+    bool have = false;
+    uint32_t issued = 0;  // tiles handed out so far (== index of the next)
+
+    __device__ bool next(int& unit, int& y) {
+        while (!have || i >= sg.ntiles) {
+            if (!walk.next(sg)) return false;
+            have = true;
+            i = 0;
+        }
+        unit = sg.b * walk.G + sg.g;
+        y = (sg.t0 + i) * kTileTokens;
+        ++i;
+        return true;
+    }
+
+    // Issues the next tile, if any, once its stage is free. Returns false when
+    // a wait gave up.
+    __device__ bool issue_one(uint32_t ring, uint32_t full_bar, uint32_t empty_bar,
+                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, const DecodeParams& p,
+                              volatile int* abort_flag, bool& done) {
+        int unit, y;
+        if (!next(unit, y)) {
+            done = true;
+            return true;
+        }
+        const uint32_t it = issued;
+        const int s = it % S;
+        if (!wait_phase(empty_bar + 8 * s, ((it / S) & 1) ^ 1, abort_flag, p.status, p.wait_timeout_ns))
+            return false;
+        issued = it + 1;
+        if (blockIdx.x == 0 && (int)it == p.skip_tile) return true;  // injected fault
+        constexpr int kStageBytes = 2 * kTileTokens * D * 2;
+        constexpr int kTileBytes = kTileTokens * D * 2;
+        const uint32_t fb = full_bar + 8 * s;
+        mbar_arrive_expect_tx(fb, kStageBytes);
+        const uint32_t kdst = ring + s * kStageBytes;
+        const uint32_t vdst = kdst + kTileBytes;
+#pragma unroll
+        for (int bx = 0; bx < D / kBoxCols; ++bx) {
+            tma_load_3d(kdst + bx * (kTileTokens * 128), tm_k, fb, bx * kBoxCols, y, unit);
+            tma_load_3d(vdst + bx * (kTileTokens * 128), tm_v, fb, bx * kBoxCols, y, unit);
+        }
+        return true;
+    }
+
+    // Waits (bounded) until the copies of tiles [consumed, issued) have landed,
+    // so that the CTA never exits with a copy into its shared memory in flight.
+    __device__ void drain(uint32_t consumed, uint32_t full_bar, const DecodeParams& p) {
+        for (uint32_t j = consumed; j < issued; ++j) {
+            if (blockIdx.x == 0 && (int)j == p.skip_tile) continue;
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(full_bar + 8 * (j % S), (j / S) & 1)) {
+                if (global_timer_ns() - t0 > p.wait_timeout_ns) {
+                    atomicOr(p.status, kStatusTimeout);
+                    break;
+                }
+            }
+        }
+    }
+};
+
 template <int D, int MT>
-__global__ void __launch_bounds__(KernelShape<D, MT>::kThreads, 1)
+__global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
     gqa_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
     using KS = KernelShape<D, MT>;
     constexpr int S = KS::kStages;
-    constexpr int NB = KS::kBoxes;
     constexpr int KSTEPS = D / 16;   // k16 steps of Q.K^T
     constexpr int NTILE_D = D / 8;   // n8 tiles of P.V (columns of O)
+    constexpr bool kQs = KS::kQInSmem;
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -107,12 +207,14 @@ __global__ void __launch_bounds__(KernelShape<D, MT>::kThreads, 1)
     unsigned char* ring_ptr = smem_raw + (ring - raw);
     float* merge_buf = reinterpret_cast<float*>(ring_ptr + S * KS::kStageBytes);
     float* ml_buf = merge_buf + KS::kMergeBytes / 4;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(ml_buf + KS::kMlBytes / 4);
+    unsigned char* q_smem = reinterpret_cast<unsigned char*>(ml_buf + KS::kMlBytes / 4);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(q_smem + KS::kQBytes);
     const uint32_t full_bar = smem_addr(bars);
     const uint32_t empty_bar = full_bar + 8 * S;
-    const uint32_t merge_bar = empty_bar + 8 * S;          // [MT][2]: A, B
-    long long* shared_ll = reinterpret_cast<long long*>(bars + 2 * S + 2 * MT);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(shared_ll + 3);
+    const uint32_t merge_bar = empty_bar + 8 * S;          // [MT][4]: A, B, C, D
+    long long* shared_ll = reinterpret_cast<long long*>(bars + 2 * S + 4 * MT);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(shared_ll + 4);
+    volatile int* last_flag = abort_flag + 1;              // [MT]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -123,48 +225,74 @@ __global__ void __launch_bounds__(KernelShape<D, MT>::kThreads, 1)
             mbar_init(full_bar + 8 * s, 1);
             mbar_init(empty_bar + 8 * s, KS::kConsumerWarps);
         }
-        for (int m = 0; m < 2 * MT; ++m) mbar_init(merge_bar + 8 * m, kSlices * 32);
+        for (int m = 0; m < 4 * MT; ++m) mbar_init(merge_bar + 8 * m, kSlices * 32);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (is_producer && lane == 0) {
+    if (threadIdx.x == KS::kConsumerWarps * 32) {
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
     }
     // Inputs may be written by the previous grid in the stream.
     pdl_wait_primary();
 
-    // Warp 0: total tiles W, and where this CTA's share starts.
+    // Warp 0: total tiles W, the number of CTAs that share them, and where
+    // this CTA's share starts. Lengths are read once; lane i keeps sequences
+    // i, i+32, ... of the first 256.
+    //
+    // When every unit has the same number of tiles (all lengths equal), the
+    // tiles are shared by fewer CTAs if a grid that keeps at least 80% of
+    // them busy lines up with the units: a whole number of units per CTA (no
+    // unit split, nothing to merge), or, with fewer units than CTAs, the same
+    // whole number of CTAs per unit (every CTA one equal partial). The CTAs
+    // left over exit.
     if (warp == 0) {
+        constexpr int kCached = 8;
+        long long cached[kCached];
         long long total = 0;
-        for (int b0 = 0; b0 < p.B; b0 += 32) {
+        int nt_min = 0x7fffffff, nt_max = 0;
+        for (int b0 = 0, k = 0; b0 < p.B; b0 += 32, ++k) {
             const int b = b0 + lane;
-            long long v = 0;
+            const int nt = b < p.B ? (int)tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Tmax)) : 0;
             if (b < p.B) {
-                const int tb = clamp_len(__ldg(p.seq_lens + b), p.Tmax);
-                v = (long long)((tb + kTileTokens - 1) / kTileTokens) * p.G;
+                nt_min = min(nt_min, nt);
+                nt_max = max(nt_max, nt);
             }
+            const long long v = (long long)nt * p.G;
+            if (k < kCached) cached[k] = v;
             long long incl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const long long n = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += n;
             }
-            if (blockIdx.x == 0 && b < p.B) p.ws_prefix[b] = total + incl - v;
             total += __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (blockIdx.x == 0 && lane == 0) p.ws_prefix[p.B] = total;
-        const long long lo = (long long)blockIdx.x * total / p.ctas;
-        // First sequence whose tiles reach past lo.
+        nt_min = __reduce_min_sync(0xffffffffu, nt_min);
+        nt_max = __reduce_max_sync(0xffffffffu, nt_max);
+        long long P = p.ctas;
+        if (p.even_rule && nt_min == nt_max && nt_max > 0) {
+            const long long units = (long long)p.B * p.G;
+            if (units >= P) {
+                const long long per = (units + P - 1) / P;
+                const long long even = (units + per - 1) / per;
+                if (units % per == 0 && 5 * even >= 4 * P) P = even;
+            } else {
+                const long long even = units * (P / units);
+                if (5 * even >= 4 * P) P = even;
+            }
+        }
+        const long long lo = (long long)blockIdx.x * total / P;
         long long pre = 0;
         int bstart = p.B;
         long long prestart = total;
-        for (int b0 = 0; b0 < p.B; b0 += 32) {
+        for (int b0 = 0, k = 0; b0 < p.B && (long long)blockIdx.x < P; b0 += 32, ++k) {
             const int b = b0 + lane;
-            long long v = 0;
-            if (b < p.B) {
-                const int tb = clamp_len(__ldg(p.seq_lens + b), p.Tmax);
-                v = (long long)((tb + kTileTokens - 1) / kTileTokens) * p.G;
+            long long v;
+            if (k < kCached) {
+                v = cached[k];
+            } else {
+                v = b < p.B ? tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Tmax)) * p.G : 0;
             }
             long long incl = v;
 #pragma unroll
@@ -185,60 +313,35 @@ __global__ void __launch_bounds__(KernelShape<D, MT>::kThreads, 1)
             shared_ll[0] = total;
             shared_ll[1] = bstart;
             shared_ll[2] = prestart;
+            shared_ll[3] = P;
         }
     }
     __syncthreads();
     pdl_launch_dependents();
 
     const long long W = shared_ll[0];
+    const long long P = shared_ll[3];   // CTAs sharing the tiles (<= gridDim.x)
     SegmentWalker walk;
     walk.seq_lens = p.seq_lens;
     walk.G = p.G;
     walk.Tmax = p.Tmax;
-    walk.lo = (long long)blockIdx.x * W / p.ctas;
-    walk.hi = (long long)(blockIdx.x + 1) * W / p.ctas;
+    walk.lo = (long long)blockIdx.x < P ? (long long)blockIdx.x * W / P : W;
+    walk.hi = (long long)blockIdx.x < P ? (long long)(blockIdx.x + 1) * W / P : W;
     walk.x = walk.lo;
     walk.b = (int)shared_ll[1];
     walk.pre_b = shared_ll[2];
 
     if (is_producer) {
-        // ------------------------------------------------------ producer
+        // ------------------------------------------ dedicated producer warp
         if (lane != 0) return;
-        uint32_t it = 0;
-        Segment sg;
-        bool ok = true;
-        while (ok && walk.next(sg)) {
-            const int unit = sg.b * p.G + sg.g;
-            for (int i = 0; i < sg.ntiles; ++i, ++it) {
-                const int s = it % S;
-                if (!wait_phase(empty_bar + 8 * s, ((it / S) & 1) ^ 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t fb = full_bar + 8 * s;
-                mbar_arrive_expect_tx(fb, KS::kStageBytes);
-                const uint32_t kdst = ring + s * KS::kStageBytes;
-                const uint32_t vdst = kdst + KS::kTileBytes;
-                const int y = (sg.t0 + i) * kTileTokens;
-#pragma unroll
-                for (int bx = 0; bx < NB; ++bx) {
-                    tma_load_3d(kdst + bx * (kTileTokens * 128), &tm_k, fb, bx * kBoxCols, y, unit);
-                    tma_load_3d(vdst + bx * (kTileTokens * 128), &tm_v, fb, bx * kBoxCols, y, unit);
-                }
-            }
-        }
-        // Leave only once every copy this warp issued has landed.
-        const uint32_t issued = it;
-        const uint32_t first = issued > (uint32_t)S ? issued - S : 0;
-        for (uint32_t j = first; j < issued; ++j) {
-            const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(full_bar + 8 * (j % S), (j / S) & 1)) {
-                if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-                    atomicOr(p.status, kStatusTimeout);
-                    break;
-                }
-            }
-        }
+        TileIssuer<D, S> issuer;
+        issuer.walk = walk;
+        bool done = false;
+        while (!done)
+            if (!issuer.issue_one(ring, full_bar, empty_bar, &tm_k, &tm_v, p, abort_flag, done)) break;
+        // Every tile but the last S was waited on through its stage's empty
+        // barrier; leave only once the copies of those last S have landed.
+        issuer.drain(issuer.issued > (uint32_t)S ? issuer.issued - S : 0, full_bar, p);
         return;
     }
 
@@ -247,10 +350,15 @@ __global__ void __launch_bounds__(KernelShape<D, MT>::kThreads, 1)
     const int mt = warp / kSlices;
     const int quad = lane & 3;
     const int grp = lane >> 2;
-    const uint32_t mbarA = merge_bar + 8 * (2 * mt);
+    const int tid_mt = slice * 32 + lane;                   // 0..127 within the row tile
+    const uint32_t mbarA = merge_bar + 8 * (4 * mt);
     const uint32_t mbarB = mbarA + 8;
-    float* my_merge = merge_buf + mt * (kSlices - 1) * 16 * D;
+    const uint32_t mbarC = mbarA + 16;
+    const uint32_t mbarD = mbarA + 24;
+    float* my_merge = merge_buf + mt * KS::kMergeFloatsPerTile;
     float* my_ml = ml_buf + mt * kSlices * 16 * 2;
+    const size_t slot_floats = ws_slot_floats(p.R, D);
+    const uint64_t tmo = p.wait_timeout_ns;
 
     // ldmatrix row addressing inside a stage (bytes from the stage base).
     // Q.K^T (B operand, non-transposed): matrix m = lane/8 -> n8 tile (m>>1),
@@ -262,15 +370,19 @@ __global__ void __launch_bounds__(KernelShape<D, MT>::kThreads, 1)
     const int v_dt = lane >> 4;
 
     uint32_t it = 0;
-    uint32_t seg_parity = 0;
+    uint32_t seg_parity = 0;   // phases of merge barriers A and B (every segment)
+    uint32_t c_parity = 0;     // phases of merge barrier C (partial segments)
+    uint32_t d_parity = 0;     // phases of merge barrier D (merges)
+    bool failed = false;
     Segment sg;
-    while (walk.next(sg)) {
+    while (!failed && walk.next(sg)) {
         // Rows of this warp's 16-row tile: r = j*sq + s (head j of the group,
-        // new token s), the fold of section 7 of the first page.
+        // new token s), the row fold of section 7 of "Same GQA, Different
+        // Execution Cost Across Backends".
         const int r_lo = mt * 16 + grp, r_hi = r_lo + 8;
         int lim_lo = sg.tb - 1, lim_hi = sg.tb - 1;
         int out_lo = -1, out_hi = -1;  // flat (b, s, h) row index for output
-        uint32_t qa[KSTEPS][4];
+        uint32_t qa[kQs ? 1 : KSTEPS][4];
         {
             const uint16_t* q_lo = nullptr;
             const uint16_t* q_hi = nullptr;
@@ -286,26 +398,48 @@ __global__ void __launch_bounds__(KernelShape<D, MT>::kThreads, 1)
                 q_hi = p.q + (size_t)out_hi * D;
                 lim_hi = sg.tb - p.sq + s;
             }
+            if constexpr (!kQs) {
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-                const int c = kk * 16 + 2 * quad;
-                qa[kk][0] = q_lo ? __ldg(reinterpret_cast<const unsigned*>(q_lo + c)) : 0u;
-                qa[kk][1] = q_hi ? __ldg(reinterpret_cast<const unsigned*>(q_hi + c)) : 0u;
-                qa[kk][2] = q_lo ? __ldg(reinterpret_cast<const unsigned*>(q_lo + c + 8)) : 0u;
-                qa[kk][3] = q_hi ? __ldg(reinterpret_cast<const unsigned*>(q_hi + c + 8)) : 0u;
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const int c = kk * 16 + 2 * quad;
+                    qa[kk][0] = q_lo ? __ldg(reinterpret_cast<const unsigned*>(q_lo + c)) : 0u;
+                    qa[kk][1] = q_hi ? __ldg(reinterpret_cast<const unsigned*>(q_hi + c)) : 0u;
+                    qa[kk][2] = q_lo ? __ldg(reinterpret_cast<const unsigned*>(q_lo + c + 8)) : 0u;
+                    qa[kk][3] = q_hi ? __ldg(reinterpret_cast<const unsigned*>(q_hi + c + 8)) : 0u;
+                }
+            } else {
+                // This warp's 16 Q rows into its own shared-memory copy, 16-byte
+                // chunks swizzled by row so that ldmatrix reads are conflict free.
+                for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
+                    const int row = idx / (D / 8), chunk = idx % (D / 8);
+                    const int r = mt * 16 + row;
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (r < p.R) {
+                        const int j = r / p.sq, sq_i = r % p.sq;
+                        const int qrow = (sg.b * p.sq + sq_i) * p.H + sg.g * p.heads_per_group + j;
+                        v = __ldg(reinterpret_cast<const uint4*>(p.q + (size_t)qrow * D) + chunk);
+                    }
+                    *reinterpret_cast<uint4*>(q_smem + warp * KS::kQBytesPerWarp + row * (D * 2) +
+                                              ((chunk ^ (row & 7)) << 4)) = v;
+                }
+                __syncwarp();
             }
         }
+        // ldmatrix of the A fragment (rows 0-7 / 8-15, k 0-7 / 8-15) of step kk.
+        const int qa_row = (lane & 7) + (((lane >> 3) & 1) << 3);
+        const uint32_t qa_base = smem_addr(q_smem) + warp * KS::kQBytesPerWarp + qa_row * (D * 2);
+        // Tiles that end at or before every row's last visible key need no mask.
+        const int lim_min = __reduce_min_sync(0xffffffffu, min(lim_lo, lim_hi));
 
         float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
         float o[NTILE_D][4];
 #pragma unroll
         for (int n = 0; n < NTILE_D; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
-        bool ok = true;
         for (int i = 0; i < sg.ntiles; ++i, ++it) {
             const int s = it % S;
-            if (!wait_phase(full_bar + 8 * s, (it / S) & 1, abort_flag, p.status)) {
-                ok = false;
+            if (!wait_phase(full_bar + 8 * s, (it / S) & 1, abort_flag, p.status, tmo)) {
+                failed = true;
                 break;
             }
             const uint32_t kst = ring + s * KS::kStageBytes;
@@ -339,20 +473,35 @@ __global__ void __launch_bounds__(KernelShape<D, MT>::kThreads, 1)
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(kst + bx * (kTileTokens * 128) + k_tok * 128 + ((cc ^ (k_tok & 7)) << 4), b0,
                         b1, b2, b3);
-                mma_bf16_16816(sc[0], qa[kk], b0, b1);
-                mma_bf16_16816(sc[1], qa[kk], b2, b3);
+                if constexpr (kQs) {
+                    const int qc = kk * 2 + (lane >> 4);
+                    uint32_t a[4];
+                    ldsm_x4(qa_base + ((qc ^ (qa_row & 7)) << 4), a[0], a[1], a[2], a[3]);
+                    mma_bf16_16816(sc[0], a, b0, b1);
+                    mma_bf16_16816(sc[1], a, b2, b3);
+                } else {
+                    mma_bf16_16816(sc[0], qa[kk], b0, b1);
+                    mma_bf16_16816(sc[1], qa[kk], b2, b3);
+                }
             }
 
             // Scale into the base-2 domain and mask invisible keys.
-            const int tok = tbase + slice * 16 + 2 * quad;
             float x[2][4];
+            if (tbase + kTileTokens - 1 <= lim_min) {
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int t = tok + 8 * j;
-                x[j][0] = (t <= lim_lo) ? sc[j][0] * p.scale_log2 : -INFINITY;
-                x[j][1] = (t + 1 <= lim_lo) ? sc[j][1] * p.scale_log2 : -INFINITY;
-                x[j][2] = (t <= lim_hi) ? sc[j][2] * p.scale_log2 : -INFINITY;
-                x[j][3] = (t + 1 <= lim_hi) ? sc[j][3] * p.scale_log2 : -INFINITY;
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) x[j][c] = sc[j][c] * p.scale_log2;
+            } else {
+                const int tok = tbase + slice * 16 + 2 * quad;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int t = tok + 8 * j;
+                    x[j][0] = (t <= lim_lo) ? sc[j][0] * p.scale_log2 : -INFINITY;
+                    x[j][1] = (t + 1 <= lim_lo) ? sc[j][1] * p.scale_log2 : -INFINITY;
+                    x[j][2] = (t <= lim_hi) ? sc[j][2] * p.scale_log2 : -INFINITY;
+                    x[j][3] = (t + 1 <= lim_hi) ? sc[j][3] * p.scale_log2 : -INFINITY;
+                }
             }
             float mx_lo = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
             float mx_hi = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
@@ -360,12 +509,16 @@ __global__ void __launch_bounds__(KernelShape<D, MT>::kThreads, 1)
             mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
             mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
             mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-            const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+            // The running max moves only when a score exceeds it by more than
+            // kRescaleSlack (base 2): until then p = 2^(x - m) stays below
+            // 2^kRescaleSlack, safe in fp32 and bf16, and the O/l rescale
+            // (a multiply of every accumulator) is skipped. The result is
+            // exact either way: O, l and m stay consistent with each other.
+            const bool up_lo = mx_lo > m_lo + kRescaleSlack;
+            const bool up_hi = mx_hi > m_hi + kRescaleSlack;
+            const float mn_lo = up_lo ? mx_lo : m_lo, mn_hi = up_hi ? mx_hi : m_hi;
             const float base_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
             const float base_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
-            const float a_lo = fast_exp2(m_lo - base_lo), a_hi = fast_exp2(m_hi - base_hi);
-            m_lo = mn_lo;
-            m_hi = mn_hi;
 
             float pr[2][4];
 #pragma unroll
@@ -375,15 +528,22 @@ __global__ void __launch_bounds__(KernelShape<D, MT>::kThreads, 1)
                 pr[j][2] = fast_exp2(x[j][2] - base_hi);
                 pr[j][3] = fast_exp2(x[j][3] - base_hi);
             }
-            l_lo = l_lo * a_lo + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
-            l_hi = l_hi * a_hi + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
+            if (__any_sync(0xffffffffu, up_lo || up_hi)) {
+                const float a_lo = fast_exp2(m_lo - base_lo), a_hi = fast_exp2(m_hi - base_hi);
+                l_lo *= a_lo;
+                l_hi *= a_hi;
 #pragma unroll
-            for (int n = 0; n < NTILE_D; ++n) {
-                o[n][0] *= a_lo;
-                o[n][1] *= a_lo;
-                o[n][2] *= a_hi;
-                o[n][3] *= a_hi;
+                for (int n = 0; n < NTILE_D; ++n) {
+                    o[n][0] *= a_lo;
+                    o[n][1] *= a_lo;
+                    o[n][2] *= a_hi;
+                    o[n][3] *= a_hi;
+                }
             }
+            m_lo = mn_lo;
+            m_hi = mn_hi;
+            l_lo += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+            l_hi += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
 
             // The S accumulator layout is the A-operand layout of P.V.
             uint32_t pa[4];
@@ -404,7 +564,7 @@ __global__ void __launch_bounds__(KernelShape<D, MT>::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar + 8 * s);
         }
-        if (!ok) return;
+        if (failed) break;
 
         // ---- merge the four slices' (m, l, O) of this row tile
         l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
@@ -418,7 +578,7 @@ __global__ void __launch_bounds__(KernelShape<D, MT>::kThreads, 1)
             my_ml[(slice * 16 + grp + 8) * 2 + 1] = l_hi;
         }
         mbar_arrive(mbarA);
-        if (!wait_phase(mbarA, seg_parity, abort_flag, p.status)) return;
+        if (!wait_phase(mbarA, seg_parity, abort_flag, p.status, tmo)) { failed = true; break; }
         float M_lo = -INFINITY, M_hi = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kSlices; ++w) {
@@ -446,28 +606,30 @@ __global__ void __launch_bounds__(KernelShape<D, MT>::kThreads, 1)
                 dst[n * 32 + lane] = make_float4(o[n][0] * f_lo, o[n][1] * f_lo, o[n][2] * f_hi, o[n][3] * f_hi);
         }
         mbar_arrive(mbarB);
-        if (!wait_phase(mbarB, seg_parity, abort_flag, p.status)) return;
+        if (!wait_phase(mbarB, seg_parity, abort_flag, p.status, tmo)) { failed = true; break; }
         seg_parity ^= 1;
-        if (slice != 0) continue;
 
-#pragma unroll
-        for (int n = 0; n < NTILE_D; ++n) {
-            o[n][0] *= f_lo;
-            o[n][1] *= f_lo;
-            o[n][2] *= f_hi;
-            o[n][3] *= f_hi;
-#pragma unroll
-            for (int w = 0; w < kSlices - 1; ++w) {
-                const float4 v = reinterpret_cast<const float4*>(my_merge + w * 16 * D)[n * 32 + lane];
-                o[n][0] += v.x;
-                o[n][1] += v.y;
-                o[n][2] += v.z;
-                o[n][3] += v.w;
-            }
-        }
         const float inv_lo = L_lo > 0.f ? 1.f / L_lo : 0.f;
         const float inv_hi = L_hi > 0.f ? 1.f / L_hi : 0.f;
+        if (slice == 0) {
+#pragma unroll
+            for (int n = 0; n < NTILE_D; ++n) {
+                o[n][0] *= f_lo;
+                o[n][1] *= f_lo;
+                o[n][2] *= f_hi;
+                o[n][3] *= f_hi;
+#pragma unroll
+                for (int w = 0; w < kSlices - 1; ++w) {
+                    const float4 v = reinterpret_cast<const float4*>(my_merge + w * 16 * D)[n * 32 + lane];
+                    o[n][0] += v.x;
+                    o[n][1] += v.y;
+                    o[n][2] += v.z;
+                    o[n][3] += v.w;
+                }
+            }
+        }
         if (sg.complete) {
+            if (slice != 0) continue;
             if (out_lo >= 0) {
                 uint16_t* orow = p.out + (size_t)out_lo * D;
 #pragma unroll
@@ -486,108 +648,168 @@ __global__ void __launch_bounds__(KernelShape<D, MT>::kThreads, 1)
                 if (p.lse && quad == 0)
                     p.lse[out_hi] = L_hi > 0.f ? (M_hi + log2f(L_hi)) * 0.69314718055994531f : -INFINITY;
             }
-        } else {
-            // Partial: O normalised by its own l, plus m and l, in slot 0 (the
-            // CTA's first segment) or 1 (its last).
-            float* slot = p.ws_part + ((size_t)blockIdx.x * 2 + (sg.first ? 0 : 1)) * ws_slot_floats(p.R, D);
+            continue;
+        }
+
+        // ---- partial segment: O normalised by its own l, plus m and l, in
+        // slot 0 (the CTA's first segment) or 1 (its last); then count the
+        // arrival. The CTA that completes the count merges the unit.
+        const long long cf = cta_of_tile(sg.ub, W, P);
+        const long long cl = cta_of_tile(sg.ue - 1, W, P);
+        if (slice == 0) {
+            float* slot = p.ws_part + ((size_t)blockIdx.x * 2 + (sg.first ? 0 : 1)) * slot_floats;
             float* om = slot + (size_t)p.R * D;
             float* ol = om + p.R;
             if (r_lo < p.R) {
 #pragma unroll
                 for (int n = 0; n < NTILE_D; ++n)
-                    *reinterpret_cast<float2*>(slot + (size_t)r_lo * D + n * 8 + 2 * quad) =
-                        make_float2(o[n][0] * inv_lo, o[n][1] * inv_lo);
+                    __stcg(reinterpret_cast<float2*>(slot + (size_t)r_lo * D + n * 8 + 2 * quad),
+                           make_float2(o[n][0] * inv_lo, o[n][1] * inv_lo));
                 if (quad == 0) {
-                    om[r_lo] = M_lo;
-                    ol[r_lo] = L_lo;
+                    __stcg(om + r_lo, M_lo);
+                    __stcg(ol + r_lo, L_lo);
                 }
             }
             if (r_hi < p.R) {
 #pragma unroll
                 for (int n = 0; n < NTILE_D; ++n)
-                    *reinterpret_cast<float2*>(slot + (size_t)r_hi * D + n * 8 + 2 * quad) =
-                        make_float2(o[n][2] * inv_hi, o[n][3] * inv_hi);
+                    __stcg(reinterpret_cast<float2*>(slot + (size_t)r_hi * D + n * 8 + 2 * quad),
+                           make_float2(o[n][2] * inv_hi, o[n][3] * inv_hi));
                 if (quad == 0) {
-                    om[r_hi] = M_hi;
-                    ol[r_hi] = L_hi;
+                    __stcg(om + r_hi, M_hi);
+                    __stcg(ol + r_hi, L_hi);
                 }
             }
-        }
-    }
-}
-
-// Merges the partials of every unit whose tiles were split across CTAs.
-// One CTA per (b, g) unit; units covered by one CTA were finished by the
-// split-KV kernel and are skipped; units with no valid key get out = 0,
-// lse = -inf.
-template <int D>
-__global__ void __launch_bounds__(256)
-    gqa_combine_kernel(const DecodeParams p) {
-    pdl_wait_primary();
-    const int unit = blockIdx.x;
-    const int b = unit / p.G, g = unit % p.G;
-    const int tb = clamp_len(__ldg(p.seq_lens + b), p.Tmax);
-    const long long nt = (tb + kTileTokens - 1) / kTileTokens;
-    constexpr int C4 = D / 4;
-    const int total = p.R * C4;
-
-    if (nt == 0) {
-        for (int i = threadIdx.x; i < total; i += blockDim.x) {
-            const int r = i / C4, c = (i % C4) * 4;
-            const int j = r / p.sq, s = r % p.sq;
-            const int row = (b * p.sq + s) * p.H + g * p.heads_per_group + j;
-            *reinterpret_cast<uint2*>(p.out + (size_t)row * D + c) = make_uint2(0u, 0u);
-            if (p.lse && c == 0) p.lse[row] = -INFINITY;
-        }
-        return;
-    }
-    const long long W = p.ws_prefix[p.B];
-    const long long ub = p.ws_prefix[b] + (long long)g * nt, ue = ub + nt;
-    const long long P = p.ctas;
-    const long long cf = ((ub + 1) * P - 1) / W;
-    const long long cl = (ue * P - 1) / W;
-    if (cf == cl) return;
-
-    const size_t slot_floats = ws_slot_floats(p.R, D);
-    for (int i = threadIdx.x; i < total; i += blockDim.x) {
-        const int r = i / C4, c = (i % C4) * 4;
-        // CTAs cf..cl cover the unit; when there are fewer tiles than CTAs some
-        // of them have an empty share and wrote no partial.
-        float M = -INFINITY;
-        for (long long cta = cf; cta <= cl; ++cta) {
-            const long long clo = cta * W / P, chi = (cta + 1) * W / P;
-            if (clo >= chi) continue;
-            const float* part = p.ws_part + ((size_t)cta * 2 + (clo >= ub ? 0 : 1)) * slot_floats;
-            M = fmaxf(M, part[(size_t)p.R * D + r]);
-        }
-        float L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (M != -INFINITY) {
-            for (long long cta = cf; cta <= cl; ++cta) {
-                const long long clo = cta * W / P, chi = (cta + 1) * W / P;
-                if (clo >= chi) continue;
-                const float* part = p.ws_part + ((size_t)cta * 2 + (clo >= ub ? 0 : 1)) * slot_floats;
-                const float m = part[(size_t)p.R * D + r];
-                const float l = part[(size_t)p.R * D + p.R + r];
-                if (m == -INFINITY || l == 0.f) continue;
-                const float w = l * fast_exp2(m - M);
-                const float4 v = *reinterpret_cast<const float4*>(part + (size_t)r * D + c);
-                L += w;
-                acc.x += w * v.x;
-                acc.y += w * v.y;
-                acc.z += w * v.z;
-                acc.w += w * v.w;
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) {
+                unsigned contributors = 0;
+                for (long long c = cf; c <= cl; ++c)
+                    contributors += (c * W / P) < ((c + 1) * W / P) ? 1u : 0u;
+                const unsigned arrived = arrive_unit(
+                    p.ws_counters + ((size_t)sg.b * p.G + sg.g) * kMaxRowTiles + mt, p.epoch, p.status);
+                __threadfence();  // the other contributors' partials are visible from here on
+                last_flag[mt] = arrived == contributors ? 1 : 0;
             }
         }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        const int j = r / p.sq, s = r % p.sq;
-        const int row = (b * p.sq + s) * p.H + g * p.heads_per_group + j;
-        uint2 packed;
-        packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-        packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(p.out + (size_t)row * D + c) = packed;
-        if (p.lse && c == 0)
-            p.lse[row] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+        mbar_arrive(mbarC);
+        if (!wait_phase(mbarC, c_parity, abort_flag, p.status, tmo)) { failed = true; break; }
+        c_parity ^= 1;
+        if (!last_flag[mt]) continue;
+        __threadfence();
+
+        // ---- this CTA arrived last: merge the unit's partials for the rows
+        // of this row tile with the log-sum-exp rescale
+        //   M = max_c m_c,  L = sum_c l_c 2^(m_c - M),  O = sum_c O_c l_c 2^(m_c - M) / L
+        // and write out and lse. The 128 threads of the row tile share the
+        // work in steps separated by a (bounded) barrier, each with one round
+        // of independent global loads: (1) the contributing slots and all
+        // their (m, l) pairs into shared memory, (2) per row the weights
+        // w_c = l_c 2^(m_c - M) / L (a warp per row, lanes over contributors),
+        // (3) the weighted sums of O.
+        {
+            int* slot_of = reinterpret_cast<int*>(my_merge);             // [ncand]
+            float* mbuf = my_merge + kMaxMergeContrib;                    // [ncand][16]
+            float* wts = mbuf + kMaxMergeContrib * 16;                    // [ncand][16]
+            const int ncand = (int)(cl - cf + 1);
+            const int rows_here = (p.R - mt * 16) < 16 ? (p.R - mt * 16) : 16;
+            for (int k = tid_mt; k < ncand; k += kSlices * 32) {
+                const long long c = cf + k;
+                const long long clo = c * W / P;
+                slot_of[k] = clo < (c + 1) * W / P ? (int)(c * 2 + (clo >= sg.ub ? 0 : 1)) : -1;
+            }
+            mbar_arrive(mbarD);
+            if (!wait_phase(mbarD, d_parity, abort_flag, p.status, tmo)) { failed = true; break; }
+            d_parity ^= 1;
+            for (int idx = tid_mt; idx < ncand * 16; idx += kSlices * 32) {
+                const int k = idx >> 4, rr = idx & 15;
+                const int sl = slot_of[k];
+                float m = -INFINITY, l = 0.f;
+                if (sl >= 0 && rr < rows_here) {
+                    const float* mp = p.ws_part + (size_t)sl * slot_floats + (size_t)p.R * D;
+                    m = __ldcg(mp + mt * 16 + rr);
+                    l = __ldcg(mp + p.R + mt * 16 + rr);
+                }
+                mbuf[idx] = m;
+                wts[idx] = l;
+            }
+            mbar_arrive(mbarD);
+            if (!wait_phase(mbarD, d_parity, abort_flag, p.status, tmo)) { failed = true; break; }
+            d_parity ^= 1;
+            for (int rr = slice; rr < rows_here; rr += kSlices) {
+                float M = -INFINITY;
+                for (int k = lane; k < ncand; k += 32) M = fmaxf(M, mbuf[k * 16 + rr]);
+#pragma unroll
+                for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+                float L = 0.f;
+                for (int k = lane; k < ncand; k += 32) {
+                    const float m = mbuf[k * 16 + rr], l = wts[k * 16 + rr];
+                    const float e = (m == -INFINITY || l == 0.f) ? 0.f : l * fast_exp2(m - M);
+                    wts[k * 16 + rr] = e;
+                    L += e;
+                }
+#pragma unroll
+                for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                for (int k = lane; k < ncand; k += 32) wts[k * 16 + rr] *= inv;
+                if (lane == 0 && p.lse) {
+                    const int r = mt * 16 + rr;
+                    const int j = r / p.sq, s = r % p.sq;
+                    const int row = (sg.b * p.sq + s) * p.H + sg.g * p.heads_per_group + j;
+                    p.lse[row] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+                }
+            }
+            mbar_arrive(mbarD);
+            if (!wait_phase(mbarD, d_parity, abort_flag, p.status, tmo)) { failed = true; break; }
+            d_parity ^= 1;
+            constexpr int C4 = D / 4;
+            for (int item = tid_mt; item < rows_here * C4; item += kSlices * 32) {
+                const int rr = item / C4;
+                const int r = mt * 16 + rr;
+                const int c4 = (item % C4) * 4;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+                for (int k = 0; k < ncand; ++k) {
+                    const int sl = slot_of[k];
+                    const float w = wts[k * 16 + rr];
+                    if (sl < 0 || w == 0.f) continue;
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                        p.ws_part + (size_t)sl * slot_floats + (size_t)r * D + c4));
+                    acc.x += w * v.x;
+                    acc.y += w * v.y;
+                    acc.z += w * v.z;
+                    acc.w += w * v.w;
+                }
+                const int j = r / p.sq, s = r % p.sq;
+                const int row = (sg.b * p.sq + s) * p.H + sg.g * p.heads_per_group + j;
+                uint2 packed;
+                packed.x = pack_bf16x2(acc.x, acc.y);
+                packed.y = pack_bf16x2(acc.z, acc.w);
+                *reinterpret_cast<uint2*>(p.out + (size_t)row * D + c4) = packed;
+            }
+            // The merge area is the slice-merge buffer of the next segment.
+            mbar_arrive(mbarD);
+            if (!wait_phase(mbarD, d_parity, abort_flag, p.status, tmo)) { failed = true; break; }
+            d_parity ^= 1;
+        }
+    }
+
+    if (failed) return;  // a wait gave up; the status word says so
+
+    // ---- sequences with no valid entry have no tile and no CTA: CTA
+    // (b mod grid) writes out = 0 and lse = -inf for all their rows.
+    {
+        const int nthreads = KS::kConsumerWarps * 32;
+        for (int b = blockIdx.x; b < p.B; b += p.ctas) {
+            if (clamp_len(__ldg(p.seq_lens + b), p.Tmax) != 0) continue;
+            const int rows = p.sq * p.H;
+            for (int i = threadIdx.x; i < rows * (D / 8); i += nthreads) {
+                const int row = b * rows + i / (D / 8);
+                const int c8 = (i % (D / 8)) * 8;
+                *reinterpret_cast<uint4*>(p.out + (size_t)row * D + c8) = make_uint4(0u, 0u, 0u, 0u);
+                if (p.lse && c8 == 0) p.lse[row] = -INFINITY;
+            }
+        }
     }
 }
 

@@ -92,6 +92,11 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
 }
 
+// Named barrier over `count` threads of the CTA (a multiple of 32).
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ----------------------------------------------------------------- misc
 // Hardware base-2 exponential (MUFU.EX2); ex2(-inf) = +0.
 __device__ __forceinline__ float fast_exp2(float x) {

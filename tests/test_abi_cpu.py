@@ -44,7 +44,7 @@ def test_plan_shapes():
     assert p["ctas"] == 152 and p["tile_tokens"] == 64 and p["row_tiles"] == 1
     assert p["max_tiles"] == 16 * 8 * 64
     assert p["smem_bytes"] <= 227 * 1024 and p["threads"] == 160
-    # MQA end: 32 rows -> two 16-row tiles and 8 consumer warps.
+    # MQA end: 32 rows -> two 16-row tiles: 8 consumer warps + 1 producer warp.
     p = gq.gqa_decode_plan(64, 1, 32, 1, 128, 8192, 152)
     assert p["row_tiles"] == 2 and p["threads"] == 288
     # A tiny problem gets at least 4 tiles per CTA.

@@ -1,0 +1,41 @@
+"""Failure detection on the GPU without a fault: every device-side wait of the
+kernel is bounded. With the test hook GQA_DECODE_DEBUG_SKIP_TILE, CTA 0 never
+loads one of its K/V tiles, so its consumers' wait for it expires (after the
+200 ms GQA_DECODE_DEBUG_TIMEOUT_MS); the kernel records that in the status
+word, waits for its own copies in flight and returns. The host must read
+GQA_ERR_DEVICE_TIMEOUT, and the context must stay usable: the next call,
+without the hook, is correct."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import grouped_query_decode_gb300 as gq
+import oracle
+from gpu_helpers import compare, make_inputs, run_gpu, to_device_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("H,G,sq", [(32, 8, 1), (64, 8, 4)], ids=["one-row-tile", "two-row-tiles"])
+def test_expired_wait_is_reported_and_the_context_survives(monkeypatch, H, G, sq):
+    B, D, Tmax = 2, 128, 700
+    q, k, v, lens = make_inputs(B, sq, H, G, D, Tmax, [700, 650], seed=77 + H)
+    dq, dk, dv = to_device_bf16(q), to_device_bf16(k), to_device_bf16(v)
+    dl = torch.from_numpy(lens).cuda()
+    out = torch.empty(B, sq, H, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, sq, H, dtype=torch.float32, device="cuda")
+    assert gq.gqa_decode_check_error() == gq.GQA_OK
+
+    monkeypatch.setenv("GQA_DECODE_DEBUG_TIMEOUT_MS", "200")
+    monkeypatch.setenv("GQA_DECODE_DEBUG_SKIP_TILE", "1")
+    gq.gqa_decode(dq, dk, dv, dl, 1 / math.sqrt(D), out, lse)
+    assert gq.gqa_decode_check_error() == gq.GQA_ERR_DEVICE_TIMEOUT
+    assert gq.gqa_decode_check_error() == gq.GQA_OK   # reading clears the word
+
+    monkeypatch.delenv("GQA_DECODE_DEBUG_SKIP_TILE")
+    monkeypatch.delenv("GQA_DECODE_DEBUG_TIMEOUT_MS")
+    ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, 1 / math.sqrt(D), threads=8)
+    got_out, got_lse = run_gpu(q, k, v, lens, 1 / math.sqrt(D), device_inputs=(dq, dk, dv, dl))
+    compare(got_out, got_lse, ref_out, ref_lse, what="after timeout")

@@ -2,12 +2,13 @@
 
 The split-KV kernel gives CTA c the tiles [c*W/P, (c+1)*W/P) of the flattened
 (sequence, KV head, 64-token tile) list; a partial result goes to slot 0 if it
-is the CTA's first segment, else slot 1; the combine kernel finds the CTAs of
-unit u as floor(((ub+1)P-1)/W) .. floor((ue*P-1)/W), skips CTAs with an empty
-share and takes slot 0 when the CTA's share starts inside the unit. This model
-restates those formulas and checks, over random ragged inputs, that every tile
-is processed once, no slot is written twice, and the combine reads exactly the
-slots the split-KV kernel wrote.
+is the CTA's first segment, else slot 1; the CTA that merges unit u finds its
+contributors as CTAs floor(((ub+1)P-1)/W) .. floor((ue*P-1)/W), skips CTAs with
+an empty share and takes slot 0 when the CTA's share starts inside the unit.
+This model restates those formulas and checks, over random ragged inputs, that
+every tile is processed once, no slot is written twice, and the merge reads
+exactly the slots that were written (and counts as many contributors as wrote
+partials for the unit).
 """
 import numpy as np
 import pytest
@@ -88,6 +89,7 @@ def test_partition_and_combine_agree(seed):
                 for r in reads:
                     assert written.get(r) == (b, g), (b, g, r)
                     read.add(r)
+                assert len(reads) == sum(1 for u in written.values() if u == (b, g))
             else:
                 assert nt[b] == 0
     assert read == set(written)   # every partial is merged, none is left over
