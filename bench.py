@@ -168,6 +168,21 @@ def _dist():
     return ws, rank, local
 
 
+def aggregate_over_ranks(ms_per_step: float, bytes_per_rank: int, device=None):
+    """Max of the per-step time over all ranks (the slowest rank sets the job's
+    pace) and the whole-job throughput: every rank processed bytes_per_rank per
+    step (weak scaling, independent replicas). Without an initialised process
+    group this is the single-GPU case."""
+    import torch
+    import torch.distributed as dist
+    ws = dist.get_world_size() if dist.is_available() and dist.is_initialized() else 1
+    if ws > 1:
+        t = torch.tensor([ms_per_step], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    return ms_per_step, ws * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------- CPU oracle
 
 def time_oracle(cfg, q, k, v, lens, budget_s: float, max_reps: int | None = None):
@@ -295,12 +310,7 @@ def run_gpu(args, cfg):
     clocks = sampler.summary()
     clocks["window"] = "timed region" if t_wall >= 0.6 else "timed region + untimed tail of the same step"
 
-    ms_step = ms_total / args.steps
-    if ws > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = ws * nbytes / (ms_step * 1e-3) / 1e9
+    ms_step, value = aggregate_over_ranks(ms_total / args.steps, nbytes, device=dev)
 
     # Per-call durations (events around each call, same stream) for the roofline.
     n_calls = min(args.steps, 200) if args.steps > 0 else 0
@@ -348,11 +358,7 @@ def run_gpu(args, cfg):
         e2e_step()
     b.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = a.elapsed_time(b) / e2e_steps
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms, e2e_value = aggregate_over_ranks(a.elapsed_time(b) / e2e_steps, nbytes, device=dev)
     h2d = hq.nbytes + hk.nbytes + hv.nbytes + hl.nbytes
     d2h = ho.nbytes + hlse.nbytes
 
@@ -386,7 +392,7 @@ def run_gpu(args, cfg):
                                      "(adds the launch gap that back-to-back launches hide)",
                          "algorithmic_bytes_per_launch": nbytes},
             "cpu_baseline": cpu,
-            "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9 * ws, "unit": "GB/s",
+            "e2e": {"value": e2e_value, "unit": "GB/s",
                     "us_per_step": e2e_ms * 1e3,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps,
