@@ -230,8 +230,8 @@ def run_reference(args, cfg):
     return 0
 
 
-def _config_dict(cfg, lens, l2_note):
-    return {"workload": cfg.name, "B": cfg.B, "sq": cfg.sq, "H": cfg.H, "G": cfg.G, "D": cfg.D,
+def _config_dict(cfg, lens, l2_note, append=False):
+    return {"workload": cfg.name + ("+append" if append else ""), "B": cfg.B, "sq": cfg.sq, "H": cfg.H, "G": cfg.G, "D": cfg.D,
             "Tmax": cfg.Tmax, "sum_T": int(np.sum(lens)), "scale": cfg.scale, "seed": cfg.seed,
             "inputs": "Q,K,V i.i.d. N(0,1) rounded to bf16", "l2": l2_note}
 
@@ -269,9 +269,18 @@ def run_gpu(args, cfg):
     lse = torch.empty(cfg.B, cfg.sq, cfg.H, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    if args.append:
+        # Fused append: each step also writes the sq new tokens' K/V rows.
+        dkn = to_dev(syn.normal_bf16(cfg.seed, 11, (cfg.B, cfg.sq, cfg.G, cfg.D)))
+        dvn = to_dev(syn.normal_bf16(cfg.seed, 12, (cfg.B, cfg.sq, cfg.G, cfg.D)))
+        nbytes += 2 * 2 * (cfg.B * cfg.sq * cfg.G * cfg.D * 2)   # new rows read + written
+
     def step(i):
         c = i % copies
-        gq.gqa_decode(dq, dks[c], dvs[c], dl, cfg.scale, out, lse, stream=stream)
+        if args.append:
+            gq.gqa_decode_append(dq, dkn, dvn, dks[c], dvs[c], dl, cfg.scale, out, lse, stream=stream)
+        else:
+            gq.gqa_decode(dq, dks[c], dvs[c], dl, cfg.scale, out, lse, stream=stream)
 
     for i in range(max(3, args.warmup)):
         step(i)
@@ -339,12 +348,21 @@ def run_gpu(args, cfg):
     hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     e2e_steps = max(3, min(args.steps, 20))
 
+    if args.append:
+        hkn = dkn.cpu().pin_memory()
+        hvn = dvn.cpu().pin_memory()
+
     def e2e_step():
         dq.copy_(hq, non_blocking=True)
         dks[0].copy_(hk, non_blocking=True)
         dvs[0].copy_(hv, non_blocking=True)
         dl.copy_(hl, non_blocking=True)
-        gq.gqa_decode(dq, dks[0], dvs[0], dl, cfg.scale, out, lse, stream=stream)
+        if args.append:
+            dkn.copy_(hkn, non_blocking=True)
+            dvn.copy_(hvn, non_blocking=True)
+            gq.gqa_decode_append(dq, dkn, dvn, dks[0], dvs[0], dl, cfg.scale, out, lse, stream=stream)
+        else:
+            gq.gqa_decode(dq, dks[0], dvs[0], dl, cfg.scale, out, lse, stream=stream)
         ho.copy_(out, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
 
@@ -360,6 +378,8 @@ def run_gpu(args, cfg):
     torch.cuda.synchronize(dev)
     e2e_ms, e2e_value = aggregate_over_ranks(a.elapsed_time(b) / e2e_steps, nbytes, device=dev)
     h2d = hq.nbytes + hk.nbytes + hv.nbytes + hl.nbytes
+    if args.append:
+        h2d += hkn.nbytes + hvn.nbytes
     d2h = ho.nbytes + hlse.nbytes
 
     line = None
@@ -376,7 +396,8 @@ def run_gpu(args, cfg):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "us_per_step": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": _config_dict(cfg, lens, l2_note=f"inputs larger than L2: {copies} rotating "
+            "config": _config_dict(cfg, lens, append=args.append,
+                                   l2_note=f"inputs larger than L2: {copies} rotating "
                                                        f"K/V copies of {cache_bytes >> 20} MiB vs "
                                                        f"{l2 >> 20} MiB L2"),
             "query_tokens_per_s": ws * cfg.B * cfg.sq / (ms_step * 1e-3),
@@ -415,6 +436,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--append", action="store_true",
+                    help="time gqa_decode_append (new K/V rows written in the same launch)")
     args = ap.parse_args(argv)
     cfg = syn.config_by_name(args.workload)
     if args.impl == "reference":

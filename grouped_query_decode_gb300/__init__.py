@@ -62,6 +62,8 @@ def load():
             lib.gqa_decode.restype = i32
             lib.gqa_decode_ex.argtypes = [vp, vp, vp, vp, f32, vp, vp, *shape, vp, sz, vp]
             lib.gqa_decode_ex.restype = i32
+            lib.gqa_decode_append.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, vp, *shape, vp]
+            lib.gqa_decode_append.restype = i32
             lib.gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, f32, vp, vp, *shape, vp]
             lib.gqa_decode_noalloc.restype = i32
             lib.gqa_decode_workspace_bytes.argtypes = shape
@@ -132,6 +134,26 @@ def gqa_decode(q, k_cache, v_cache, seq_lens, scale, out, lse=None, stream=None)
                            _stream_handle(stream, q.device))
     if rc != GQA_OK:
         raise GQADecodeError(rc, "gqa_decode")
+
+
+def gqa_decode_append(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out, lse=None,
+                      stream=None):
+    """One decode step that first appends the sq new tokens' K/V ([B, sq, G, D]
+    bf16) to the caches at positions seq_lens[b] - sq + s, in the same launch."""
+    B, sq, H, G, D, Tmax = _shapes(q, k_cache, v_cache, seq_lens, out, lse)
+    import torch
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+        if tuple(t.shape) != (B, sq, G, D):
+            raise ValueError(f"{name} must be [B, sq, G, D]")
+    rc = load().gqa_decode_append(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                  k_cache.data_ptr(), v_cache.data_ptr(), seq_lens.data_ptr(),
+                                  float(scale), out.data_ptr(),
+                                  None if lse is None else lse.data_ptr(), B, sq, H, G, D, Tmax,
+                                  _stream_handle(stream, q.device))
+    if rc != GQA_OK:
+        raise GQADecodeError(rc, "gqa_decode_append")
 
 
 def gqa_decode_ex(q, k_cache, v_cache, seq_lens, scale, out, lse, workspace, stream=None):

@@ -183,15 +183,23 @@ size_t gqa_decode_workspace_bytes(int B, int sq, int H, int G, int D, int Tmax) 
     return ws_total_bytes(B, G, (H / G) * sq, D, plan.ctas);
 }
 
-int gqa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
-                  const int32_t* seq_lens, float scale, void* out, float* lse, int B, int sq,
-                  int H, int G, int D, int Tmax, void* workspace, size_t workspace_bytes,
-                  cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks the arguments, builds the TMA descriptors and the kernel parameters,
+// and enqueues the one launch of a decode step (with the fused append when
+// k_new/v_new are given).
+int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
+            float scale, void* out, float* lse, int B, int sq, int H, int G, int D, int Tmax,
+            void* workspace, size_t workspace_bytes, cudaStream_t stream, const void* k_new,
+            const void* v_new) {
     if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_INVALID_ARG;
     int st = check_shapes(B, sq, H, G, D, Tmax);
     if (st != GQA_OK) return st;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(seq_lens) ||
-        !aligned16(out) || (lse && !aligned16(lse)))
+        !aligned16(out) || (lse && !aligned16(lse)) || (k_new && !aligned16(k_new)) ||
+        (v_new && !aligned16(v_new)))
         return GQA_ERR_MISALIGNED;
     DeviceInfo info;
     st = device_info(&info);
@@ -228,12 +236,53 @@ int gqa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
     a.p.ctas = plan.ctas;
     a.p.even_rule = forced_ctas() > 0 ? 0 : 1;
     debug_knobs(&a.p.wait_timeout_ns, &a.p.skip_tile);
+    a.p.k_new = static_cast<const uint16_t*>(k_new);
+    a.p.v_new = static_cast<const uint16_t*>(v_new);
+    a.p.k_cache = static_cast<uint16_t*>(const_cast<void*>(k_cache));
+    a.p.v_cache = static_cast<uint16_t*>(const_cast<void*>(v_cache));
     a.row_tiles = plan.row_tiles;
     a.pdl = true;
     a.stream = stream;
     cudaError_t e = D == 64 ? launch_d64(a) : launch_d128(a);
     if (e != cudaSuccess) return cuda_fail(e);
     return GQA_OK;
+}
+
+// The library-owned workspace of (current device, stream), grown to `need`.
+int stream_workspace(cudaStream_t stream, size_t need, void** ws, size_t* have) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto& slot = g_workspaces[{dev, stream}];
+    if (slot.second < need) {
+        if (slot.first) {
+            // The old buffer may still be in use by work queued on this stream.
+            e = cudaStreamSynchronize(stream);
+            if (e != cudaSuccess) return cuda_fail(e);
+            cudaFree(slot.first);
+            slot = {nullptr, 0};
+        }
+        void* p = nullptr;
+        e = cudaMalloc(&p, need);
+        if (e != cudaSuccess) return cuda_fail(e);
+        slot = {p, need};
+    }
+    *ws = slot.first;
+    *have = slot.second;
+    return GQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gqa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* seq_lens, float scale, void* out, float* lse, int B, int sq,
+                  int H, int G, int D, int Tmax, void* workspace, size_t workspace_bytes,
+                  cudaStream_t stream) {
+    return enqueue(q, k_cache, v_cache, seq_lens, scale, out, lse, B, sq, H, G, D, Tmax, workspace,
+                   workspace_bytes, stream, nullptr, nullptr);
 }
 
 int gqa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
@@ -244,32 +293,29 @@ int gqa_decode(const void* q, const void* k_cache, const void* v_cache, const in
     if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_INVALID_ARG;
     const size_t need = gqa_decode_workspace_bytes(B, sq, H, G, D, Tmax);
     if (need == 0) return GQA_ERR_CUDA;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e);
     void* ws = nullptr;
     size_t have = 0;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        auto& slot = g_workspaces[{dev, stream}];
-        if (slot.second < need) {
-            if (slot.first) {
-                // The old buffer may still be in use by work queued on this stream.
-                e = cudaStreamSynchronize(stream);
-                if (e != cudaSuccess) return cuda_fail(e);
-                cudaFree(slot.first);
-                slot = {nullptr, 0};
-            }
-            void* p = nullptr;
-            e = cudaMalloc(&p, need);
-            if (e != cudaSuccess) return cuda_fail(e);
-            slot = {p, need};
-        }
-        ws = slot.first;
-        have = slot.second;
-    }
-    return gqa_decode_ex(q, k_cache, v_cache, seq_lens, scale, out, lse, B, sq, H, G, D, Tmax, ws,
-                         have, stream);
+    st = stream_workspace(stream, need, &ws, &have);
+    if (st != GQA_OK) return st;
+    return enqueue(q, k_cache, v_cache, seq_lens, scale, out, lse, B, sq, H, G, D, Tmax, ws, have,
+                   stream, nullptr, nullptr);
+}
+
+int gqa_decode_append(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                      void* v_cache, const int32_t* seq_lens, float scale, void* out, float* lse,
+                      int B, int sq, int H, int G, int D, int Tmax, cudaStream_t stream) {
+    int st = check_shapes(B, sq, H, G, D, Tmax);
+    if (st != GQA_OK) return st;
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !seq_lens || !out)
+        return GQA_ERR_INVALID_ARG;
+    const size_t need = gqa_decode_workspace_bytes(B, sq, H, G, D, Tmax);
+    if (need == 0) return GQA_ERR_CUDA;
+    void* ws = nullptr;
+    size_t have = 0;
+    st = stream_workspace(stream, need, &ws, &have);
+    if (st != GQA_OK) return st;
+    return enqueue(q, k_cache, v_cache, seq_lens, scale, out, lse, B, sq, H, G, D, Tmax, ws, have,
+                   stream, k_new, v_new);
 }
 
 int gqa_decode_check_error(cudaStream_t stream) {

@@ -51,6 +51,12 @@ struct DecodeParams {
     int even_rule;           // 1: use fewer CTAs when that splits no unit (see kernel)
     int skip_tile;           // fault injection for tests: CTA 0 never loads its tile
                              // number skip_tile (-1: off), so its consumers' wait expires
+    // Fused append (all null for a plain decode): the sq new tokens' K/V,
+    // [B, sq, G, D] bf16, go to cache positions T_b - sq + s before attending.
+    const uint16_t* k_new;
+    const uint16_t* v_new;
+    uint16_t* k_cache;       // the caches, for writing the new rows
+    uint16_t* v_cache;
 };
 
 // One CTA per SM. Every 16-row tile of the group has four consumer warps

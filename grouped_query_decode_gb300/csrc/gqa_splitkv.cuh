@@ -464,6 +464,39 @@ __global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
                 __syncwarp();
             }
 
+            // Fused append: the new tokens' rows of this warp's 16-token slice
+            // come from k_new/v_new, not from the cache the TMA just read. The
+            // warp patches them into the stage before reading it and (one row
+            // tile's warp) stores them to the cache. Each position lies in
+            // exactly one tile, which one CTA owns, so no other CTA reads it.
+            if (p.k_new != nullptr) {
+                const int new_lo = sg.tb - p.sq;
+                const int lo = max(new_lo, tbase + slice * 16);
+                const int hi = min(sg.tb, tbase + slice * 16 + 16);
+                if (lo < hi) {
+                    const size_t unit_row0 = ((size_t)sg.b * p.G + sg.g) * p.Tmax;
+                    for (int idx = lane; idx < (hi - lo) * (D / 8); idx += 32) {
+                        const int t = lo + idx / (D / 8);
+                        const int chunk = idx % (D / 8);
+                        const size_t src = (((size_t)sg.b * p.sq + (t - new_lo)) * p.G + sg.g) * D + chunk * 8;
+                        const uint4 kv = __ldg(reinterpret_cast<const uint4*>(p.k_new + src));
+                        const uint4 vv = __ldg(reinterpret_cast<const uint4*>(p.v_new + src));
+                        const int row = t - tbase;
+                        const uint32_t off = (chunk >> 3) * (kTileTokens * 128) + row * 128 +
+                                             (((chunk & 7) ^ (row & 7)) << 4);
+                        st_shared_v4(kst + off, kv);
+                        st_shared_v4(vst + off, vv);
+                        if (mt == 0) {
+                            const size_t dst = (unit_row0 + t) * D + chunk * 8;
+                            *reinterpret_cast<uint4*>(p.k_cache + dst) = kv;
+                            *reinterpret_cast<uint4*>(p.v_cache + dst) = vv;
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+            }
+
             // S = Q K^T for this warp's 16 tokens: two n8 tiles.
             float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll

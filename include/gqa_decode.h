@@ -85,6 +85,27 @@ int gqa_decode(const void* q, const void* k_cache, const void* v_cache,
                int B, int sq, int H, int G, int D, int Tmax, cudaStream_t stream);
 
 /*
+ * Decode step with the new tokens' K/V appended to the cache in the same
+ * launch: the per-layer step of "GQA analysis", section "Incremental decode",
+ * which appends k_t and v_t to the caches and then attends over them.
+ *
+ * k_new, v_new: [B, sq, G, D] bf16, device, 16-byte aligned -- the sq new
+ * tokens' keys (already rotated, if the model uses RoPE) and values per KV
+ * head. seq_lens counts the cache entries including the new ones, as for
+ * gqa_decode: new token s of sequence b is written to
+ * k_cache[b, g, T_b - sq + s, :] (T_b clamped to [0, Tmax]; positions below 0
+ * are not written) and v_cache likewise; every other cache entry is left as
+ * it is. The result is the same as writing those rows first and then calling
+ * gqa_decode; the rows are written by the same launch, which reads them from
+ * k_new/v_new rather than back from the cache. Library-owned workspace, as for
+ * gqa_decode. The caches must not be read or written by other work until the
+ * call has completed on `stream`.
+ */
+int gqa_decode_append(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                      void* v_cache, const int32_t* seq_lens, float scale, void* out, float* lse,
+                      int B, int sq, int H, int G, int D, int Tmax, cudaStream_t stream);
+
+/*
  * Bytes of device workspace gqa_decode_ex needs for these sizes on the current
  * device: two partial-result slots (O[R][D], running max m[R], sum l[R]) per
  * split-KV CTA plus the per-sequence tile prefix sums. Returns 0 for

@@ -97,6 +97,35 @@ class Oracle:
         return out, lse
 
 
+def append_f64(k_cache, v_cache, k_new, v_new, seq_lens):
+    """The cache update of "GQA analysis", sections "Projection and RoPE" and
+    "Incremental decode" (append(K_cache, K_t); append(V_cache, V_t)): new
+    token s of sequence b goes to position T_b - sq + s of every KV head, where
+    T_b = seq_lens[b] counts the entries including the new ones; positions
+    below 0 are dropped. Returns updated copies; k_new/v_new are [B, sq, G, D]
+    bf16 bits, the caches [B, G, Tmax, D]."""
+    k = np.array(k_cache, dtype=np.uint16, copy=True)
+    v = np.array(v_cache, dtype=np.uint16, copy=True)
+    B, G, Tmax, D = k.shape
+    sq = k_new.shape[1]
+    for b in range(B):
+        T = int(seq_lens[b])
+        for s in range(sq):
+            t = T - sq + s
+            if 0 <= t < Tmax:
+                k[b, :, t, :] = k_new[b, s]
+                v[b, :, t, :] = v_new[b, s]
+    return k, v
+
+
+def gqa_decode_append_f64(q, k_cache, v_cache, k_new, v_new, seq_lens, scale, threads: int = 1):
+    """Append the new tokens' K/V (append_f64), then the decode definition over
+    the updated caches. Returns (out, lse, k_cache_after, v_cache_after)."""
+    k, v = append_f64(k_cache, v_cache, k_new, v_new, seq_lens)
+    out, lse = get().gqa_decode(q, k, v, seq_lens, scale, threads=threads)
+    return out, lse, k, v
+
+
 def get() -> Oracle:
     """The oracle built from gqa_oracle.c (compiled on first use)."""
     global _default
