@@ -230,8 +230,8 @@ def run_reference(args, cfg):
     return 0
 
 
-def _config_dict(cfg, lens, l2_note, append=False):
-    return {"workload": cfg.name + ("+append" if append else ""), "B": cfg.B, "sq": cfg.sq, "H": cfg.H, "G": cfg.G, "D": cfg.D,
+def _config_dict(cfg, lens, l2_note, append=False, paged=0):
+    return {"workload": cfg.name + ("+append" if append else "") + (f"+paged{paged}" if paged else ""), "B": cfg.B, "sq": cfg.sq, "H": cfg.H, "G": cfg.G, "D": cfg.D,
             "Tmax": cfg.Tmax, "sum_T": int(np.sum(lens)), "scale": cfg.scale, "seed": cfg.seed,
             "inputs": "Q,K,V i.i.d. N(0,1) rounded to bf16", "l2": l2_note}
 
@@ -275,9 +275,25 @@ def run_gpu(args, cfg):
         dvn = to_dev(syn.normal_bf16(cfg.seed, 12, (cfg.B, cfg.sq, cfg.G, cfg.D)))
         nbytes += 2 * 2 * (cfg.B * cfg.sq * cfg.G * cfg.D * 2)   # new rows read + written
 
+    if args.paged:
+        # The same logical caches laid out in pages, one paged copy per
+        # rotation slot, each with its own block table.
+        paged = []
+        for c in range(copies):
+            kp, vp, table = syn.paginate(k, v, lens, args.paged, seed=cfg.seed + 100 + c,
+                                         fill_bits=syn.BF16_ZERO)
+            paged.append((to_dev(kp), to_dev(vp), torch.from_numpy(table).to(dev)))
+            if c == 0:
+                host_paged = (kp, vp, table)
+        del dks[:], dvs[:]
+        nbytes += sum(-(-int(t) // args.paged) for t in lens) * 4     # block-table entries read
+
     def step(i):
         c = i % copies
-        if args.append:
+        if args.paged:
+            kp_, vp_, tb_ = paged[c]
+            gq.gqa_decode_paged(dq, kp_, vp_, tb_, dl, cfg.scale, out, lse, stream=stream)
+        elif args.append:
             gq.gqa_decode_append(dq, dkn, dvn, dks[c], dvs[c], dl, cfg.scale, out, lse, stream=stream)
         else:
             gq.gqa_decode(dq, dks[c], dvs[c], dl, cfg.scale, out, lse, stream=stream)
@@ -341,8 +357,15 @@ def run_gpu(args, cfg):
 
     # End to end: inputs from pinned host memory, outputs back, every step.
     hq = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hk = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hv = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+    if args.paged:
+        hk = torch.from_numpy(host_paged[0].view(np.int16)).view(torch.bfloat16).pin_memory()
+        hv = torch.from_numpy(host_paged[1].view(np.int16)).view(torch.bfloat16).pin_memory()
+        htab = torch.from_numpy(host_paged[2]).pin_memory()
+        e2e_k, e2e_v, e2e_t = paged[0]
+    else:
+        hk = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hv = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+        e2e_k, e2e_v = dks[0], dvs[0]
     hl = torch.from_numpy(lens).pin_memory()
     ho = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
     hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
@@ -354,15 +377,18 @@ def run_gpu(args, cfg):
 
     def e2e_step():
         dq.copy_(hq, non_blocking=True)
-        dks[0].copy_(hk, non_blocking=True)
-        dvs[0].copy_(hv, non_blocking=True)
+        e2e_k.copy_(hk, non_blocking=True)
+        e2e_v.copy_(hv, non_blocking=True)
         dl.copy_(hl, non_blocking=True)
-        if args.append:
+        if args.paged:
+            e2e_t.copy_(htab, non_blocking=True)
+            gq.gqa_decode_paged(dq, e2e_k, e2e_v, e2e_t, dl, cfg.scale, out, lse, stream=stream)
+        elif args.append:
             dkn.copy_(hkn, non_blocking=True)
             dvn.copy_(hvn, non_blocking=True)
-            gq.gqa_decode_append(dq, dkn, dvn, dks[0], dvs[0], dl, cfg.scale, out, lse, stream=stream)
+            gq.gqa_decode_append(dq, dkn, dvn, e2e_k, e2e_v, dl, cfg.scale, out, lse, stream=stream)
         else:
-            gq.gqa_decode(dq, dks[0], dvs[0], dl, cfg.scale, out, lse, stream=stream)
+            gq.gqa_decode(dq, e2e_k, e2e_v, dl, cfg.scale, out, lse, stream=stream)
         ho.copy_(out, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
 
@@ -377,7 +403,7 @@ def run_gpu(args, cfg):
     b.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms, e2e_value = aggregate_over_ranks(a.elapsed_time(b) / e2e_steps, nbytes, device=dev)
-    h2d = hq.nbytes + hk.nbytes + hv.nbytes + hl.nbytes
+    h2d = hq.nbytes + hk.nbytes + hv.nbytes + hl.nbytes + (htab.nbytes if args.paged else 0)
     if args.append:
         h2d += hkn.nbytes + hvn.nbytes
     d2h = ho.nbytes + hlse.nbytes
@@ -396,7 +422,7 @@ def run_gpu(args, cfg):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "us_per_step": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": _config_dict(cfg, lens, append=args.append,
+            "config": _config_dict(cfg, lens, append=args.append, paged=args.paged,
                                    l2_note=f"inputs larger than L2: {copies} rotating "
                                                        f"K/V copies of {cache_bytes >> 20} MiB vs "
                                                        f"{l2 >> 20} MiB L2"),
@@ -436,6 +462,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--paged", type=int, default=0, metavar="PAGE_SIZE",
+                    help="time gqa_decode_paged on the same caches split into pages of this size")
     ap.add_argument("--append", action="store_true",
                     help="time gqa_decode_append (new K/V rows written in the same launch)")
     args = ap.parse_args(argv)

@@ -64,6 +64,8 @@ def load():
             lib.gqa_decode_ex.restype = i32
             lib.gqa_decode_append.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, vp, *shape, vp]
             lib.gqa_decode_append.restype = i32
+            lib.gqa_decode_paged.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, *([i32] * 8), vp]
+            lib.gqa_decode_paged.restype = i32
             lib.gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, f32, vp, vp, *shape, vp]
             lib.gqa_decode_noalloc.restype = i32
             lib.gqa_decode_workspace_bytes.argtypes = shape
@@ -154,6 +156,35 @@ def gqa_decode_append(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out, l
                                   _stream_handle(stream, q.device))
     if rc != GQA_OK:
         raise GQADecodeError(rc, "gqa_decode_append")
+
+
+def gqa_decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale, out, lse=None,
+                     stream=None):
+    """One decode step over a paged cache: k_pages/v_pages [num_pages, G,
+    page_size, D] bf16, block_table [B, max_pages_per_seq] int32."""
+    import torch
+    for name, t, dt in (("q", q, torch.bfloat16), ("k_pages", k_pages, torch.bfloat16),
+                        ("v_pages", v_pages, torch.bfloat16), ("block_table", block_table, torch.int32),
+                        ("seq_lens", seq_lens, torch.int32), ("out", out, torch.bfloat16)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous {dt} CUDA tensor")
+    B, sq, H, D = q.shape
+    num_pages, G, page_size, Dk = k_pages.shape
+    if Dk != D or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("k_pages / v_pages must be [num_pages, G, page_size, D]")
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_pages_per_seq]")
+    if tuple(seq_lens.shape) != (B,) or tuple(out.shape) != (B, sq, H, D):
+        raise ValueError("seq_lens must be [B] and out [B, sq, H, D]")
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, sq, H)):
+        raise ValueError("lse must be float32 [B, sq, H]")
+    rc = load().gqa_decode_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                                 block_table.data_ptr(), seq_lens.data_ptr(), float(scale),
+                                 out.data_ptr(), None if lse is None else lse.data_ptr(),
+                                 B, sq, H, G, D, page_size, num_pages, block_table.shape[1],
+                                 _stream_handle(stream, q.device))
+    if rc != GQA_OK:
+        raise GQADecodeError(rc, "gqa_decode_paged")
 
 
 def gqa_decode_ex(q, k_cache, v_cache, seq_lens, scale, out, lse, workspace, stream=None):

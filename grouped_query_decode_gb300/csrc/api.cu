@@ -75,14 +75,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// A [B*G units][Tmax][D] bf16 cache viewed as a 3-D tensor; boxes of 64 rows x
-// 64 elements (128 bytes) with the 128-byte swizzle. Rows past Tmax read as 0.
-int encode_cache_map(CUtensorMap* map, const void* base, int B, int G, int Tmax, int D) {
+// A cache of `slabs` slabs of [rows][D] bf16 -- [B*G units][Tmax][D] for a
+// contiguous cache, [pages*G][page_size][D] for a paged one -- viewed as a 3-D
+// tensor; boxes of box_rows rows x 64 elements (128 bytes) with the 128-byte
+// swizzle. Reads past a slab's rows, or of a slab out of range, give 0.
+int encode_cache_map(CUtensorMap* map, const void* base, long long slabs, int rows, int D,
+                     int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return cuda_fail(cudaErrorNotSupported);
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Tmax, (cuuint64_t)B * G};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Tmax * D * 2};
-    cuuint32_t box[3] = {(cuuint32_t)kBoxCols, (cuuint32_t)kTileTokens, 1};
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)slabs};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows * D * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kBoxCols, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -190,10 +193,15 @@ namespace {
 // Checks the arguments, builds the TMA descriptors and the kernel parameters,
 // and enqueues the one launch of a decode step (with the fused append when
 // k_new/v_new are given).
+struct Paging {
+    const int32_t* block_table = nullptr;  // null: contiguous cache
+    int page_size = 0, num_pages = 0, max_pages = 0;
+};
+
 int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
             float scale, void* out, float* lse, int B, int sq, int H, int G, int D, int Tmax,
             void* workspace, size_t workspace_bytes, cudaStream_t stream, const void* k_new,
-            const void* v_new) {
+            const void* v_new, const Paging& pg = Paging()) {
     if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_INVALID_ARG;
     int st = check_shapes(B, sq, H, G, D, Tmax);
     if (st != GQA_OK) return st;
@@ -213,9 +221,12 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32
         return GQA_ERR_WORKSPACE;
 
     LaunchArgs a;
-    st = encode_cache_map(&a.tm_k, k_cache, B, G, Tmax, D);
+    const long long slabs = pg.block_table ? (long long)pg.num_pages * G : (long long)B * G;
+    const int rows = pg.block_table ? pg.page_size : Tmax;
+    const int box_rows = pg.block_table && pg.page_size < kTileTokens ? pg.page_size : kTileTokens;
+    st = encode_cache_map(&a.tm_k, k_cache, slabs, rows, D, box_rows);
     if (st != GQA_OK) return st;
-    st = encode_cache_map(&a.tm_v, v_cache, B, G, Tmax, D);
+    st = encode_cache_map(&a.tm_v, v_cache, slabs, rows, D, box_rows);
     if (st != GQA_OK) return st;
     a.p.q = static_cast<const uint16_t*>(q);
     a.p.seq_lens = seq_lens;
@@ -240,6 +251,9 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32
     a.p.v_new = static_cast<const uint16_t*>(v_new);
     a.p.k_cache = static_cast<uint16_t*>(const_cast<void*>(k_cache));
     a.p.v_cache = static_cast<uint16_t*>(const_cast<void*>(v_cache));
+    a.p.block_table = pg.block_table;
+    a.p.page_size = pg.page_size;
+    a.p.max_pages = pg.max_pages;
     a.row_tiles = plan.row_tiles;
     a.pdl = true;
     a.stream = stream;
@@ -316,6 +330,36 @@ int gqa_decode_append(const void* q, const void* k_new, const void* v_new, void*
     if (st != GQA_OK) return st;
     return enqueue(q, k_cache, v_cache, seq_lens, scale, out, lse, B, sq, H, G, D, Tmax, ws, have,
                    stream, k_new, v_new);
+}
+
+int gqa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                     const int32_t* block_table, const int32_t* seq_lens, float scale, void* out,
+                     float* lse, int B, int sq, int H, int G, int D, int page_size, int num_pages,
+                     int max_pages_per_seq, cudaStream_t stream) {
+    if (page_size < 8 || page_size > 65536 || (page_size & (page_size - 1)) || num_pages <= 0 ||
+        max_pages_per_seq <= 0)
+        return page_size <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 ? GQA_ERR_INVALID_ARG
+                                                                           : GQA_ERR_UNSUPPORTED;
+    const long long tmax = (long long)max_pages_per_seq * page_size;
+    if (tmax >= (1ll << 31) || (long long)num_pages * G >= (1ll << 31)) return GQA_ERR_UNSUPPORTED;
+    const int Tmax = (int)tmax;
+    int st = check_shapes(B, sq, H, G, D, Tmax);
+    if (st != GQA_OK) return st;
+    if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !out) return GQA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(block_table) & 3u) return GQA_ERR_MISALIGNED;
+    const size_t need = gqa_decode_workspace_bytes(B, sq, H, G, D, Tmax);
+    if (need == 0) return GQA_ERR_CUDA;
+    void* ws = nullptr;
+    size_t have = 0;
+    st = stream_workspace(stream, need, &ws, &have);
+    if (st != GQA_OK) return st;
+    Paging pg;
+    pg.block_table = block_table;
+    pg.page_size = page_size;
+    pg.num_pages = num_pages;
+    pg.max_pages = max_pages_per_seq;
+    return enqueue(q, k_pages, v_pages, seq_lens, scale, out, lse, B, sq, H, G, D, Tmax, ws, have,
+                   stream, nullptr, nullptr, pg);
 }
 
 int gqa_decode_check_error(cudaStream_t stream) {

@@ -57,6 +57,11 @@ struct DecodeParams {
     const uint16_t* v_new;
     uint16_t* k_cache;       // the caches, for writing the new rows
     uint16_t* v_cache;
+    // Paged caches (null block_table for a contiguous cache): K/V pages
+    // [num_pages, G, page_size, D]; block_table [B, max_pages] maps logical
+    // page j of sequence b to its physical page.
+    const int32_t* block_table;
+    int page_size, max_pages;
 };
 
 // One CTA per SM. Every 16-row tile of the group has four consumer warps

@@ -122,9 +122,20 @@ __device__ __forceinline__ long long cta_of_tile(long long x, long long W, long 
     return ((x + 1) * P - 1) / W;
 }
 
+// One tile of the CTA's share, with where its rows live. For a paged cache a
+// 64-token tile covers part of one page (pages of >= 64 tokens) or
+// 64 / page_size whole pages; `page` holds their physical numbers (pages that
+// start at or past the sequence's length are not looked up and stay -1).
+struct TileRef {
+    int unit, g, tb, t;      // unit = b*G + g; t = tile index within the unit
+    int page[4];
+};
+
 // Hands out the CTA's tiles in order and issues their TMA copies into the
 // ring: stage it % S, armed on full[it % S] once empty[it % S] shows that the
-// consumers are done with the tile S places earlier.
+// consumers are done with the tile S places earlier. The next tile is looked
+// up one step ahead, so that its block-table reads (paged caches) are in
+// flight while the producer waits for a free stage.
 template <int D, int S>
 struct TileIssuer {
     SegmentWalker walk;
@@ -132,29 +143,47 @@ struct TileIssuer {
     int i = 0;
     bool have = false;
     uint32_t issued = 0;  // tiles handed out so far (== index of the next)
+    TileRef cur;
+    bool have_cur = false;
 
-    __device__ bool next(int& unit, int& y) {
+    __device__ bool next(const DecodeParams& p, TileRef& r) {
         while (!have || i >= sg.ntiles) {
             if (!walk.next(sg)) return false;
             have = true;
             i = 0;
         }
-        unit = sg.b * walk.G + sg.g;
-        y = (sg.t0 + i) * kTileTokens;
+        r.unit = sg.b * walk.G + sg.g;
+        r.g = sg.g;
+        r.tb = sg.tb;
+        r.t = sg.t0 + i;
         ++i;
+        r.page[0] = r.page[1] = r.page[2] = r.page[3] = -1;
+        if (p.block_table != nullptr) {
+            const int32_t* bt = p.block_table + (size_t)sg.b * p.max_pages;
+            const int tok0 = r.t * kTileTokens;
+            if (p.page_size >= kTileTokens) {
+                r.page[0] = __ldg(bt + tok0 / p.page_size);
+            } else {
+                for (int j = 0; j < kTileTokens / p.page_size; ++j)
+                    if (tok0 + j * p.page_size < r.tb) r.page[j] = __ldg(bt + tok0 / p.page_size + j);
+            }
+        }
         return true;
     }
 
-    // Issues the next tile, if any, once its stage is free. Returns false when
-    // a wait gave up.
+    __device__ void start(const DecodeParams& p) { have_cur = next(p, cur); }
+
+    // Issues the current tile, if any, once its stage is free, and looks up
+    // the one after it. Returns false when a wait gave up.
     __device__ bool issue_one(uint32_t ring, uint32_t full_bar, uint32_t empty_bar,
                               const CUtensorMap* tm_k, const CUtensorMap* tm_v, const DecodeParams& p,
                               volatile int* abort_flag, bool& done) {
-        int unit, y;
-        if (!next(unit, y)) {
+        if (!have_cur) {
             done = true;
             return true;
         }
+        const TileRef r = cur;
+        have_cur = next(p, cur);
         const uint32_t it = issued;
         const int s = it % S;
         if (!wait_phase(empty_bar + 8 * s, ((it / S) & 1) ^ 1, abort_flag, p.status, p.wait_timeout_ns))
@@ -163,14 +192,46 @@ struct TileIssuer {
         if (blockIdx.x == 0 && (int)it == p.skip_tile) return true;  // injected fault
         constexpr int kStageBytes = 2 * kTileTokens * D * 2;
         constexpr int kTileBytes = kTileTokens * D * 2;
+        constexpr int NB = D / kBoxCols;
         const uint32_t fb = full_bar + 8 * s;
-        mbar_arrive_expect_tx(fb, kStageBytes);
         const uint32_t kdst = ring + s * kStageBytes;
         const uint32_t vdst = kdst + kTileBytes;
+        if (p.block_table == nullptr) {
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            const int y = r.t * kTileTokens;
 #pragma unroll
-        for (int bx = 0; bx < D / kBoxCols; ++bx) {
-            tma_load_3d(kdst + bx * (kTileTokens * 128), tm_k, fb, bx * kBoxCols, y, unit);
-            tma_load_3d(vdst + bx * (kTileTokens * 128), tm_v, fb, bx * kBoxCols, y, unit);
+            for (int bx = 0; bx < NB; ++bx) {
+                tma_load_3d(kdst + bx * (kTileTokens * 128), tm_k, fb, bx * kBoxCols, y, r.unit);
+                tma_load_3d(vdst + bx * (kTileTokens * 128), tm_v, fb, bx * kBoxCols, y, r.unit);
+            }
+        } else if (p.page_size >= kTileTokens) {
+            // One box of 64 rows inside page r.page[0]: tensor map [D, page_size, pages*G].
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            const int y = (r.t * kTileTokens) % p.page_size;
+            const int z = r.page[0] * p.G + r.g;
+#pragma unroll
+            for (int bx = 0; bx < NB; ++bx) {
+                tma_load_3d(kdst + bx * (kTileTokens * 128), tm_k, fb, bx * kBoxCols, y, z);
+                tma_load_3d(vdst + bx * (kTileTokens * 128), tm_v, fb, bx * kBoxCols, y, z);
+            }
+        } else {
+            // One box of page_size rows per page that starts before the end of
+            // the sequence; rows past the length are never used (masked, and
+            // zeroed in V), so the pages after the last one are not read.
+            const int ps = p.page_size;
+            int npages = 0;
+            for (int j = 0; j < kTileTokens / ps; ++j) npages += r.page[j] >= 0 ? 1 : 0;
+            mbar_arrive_expect_tx(fb, (uint32_t)npages * NB * ps * 128 * 2);
+            for (int j = 0; j < kTileTokens / ps; ++j) {
+                if (r.page[j] < 0) continue;
+                const int z = r.page[j] * p.G + r.g;
+#pragma unroll
+                for (int bx = 0; bx < NB; ++bx) {
+                    const uint32_t off = bx * (kTileTokens * 128) + j * ps * 128;
+                    tma_load_3d(kdst + off, tm_k, fb, bx * kBoxCols, 0, z);
+                    tma_load_3d(vdst + off, tm_v, fb, bx * kBoxCols, 0, z);
+                }
+            }
         }
         return true;
     }
@@ -336,6 +397,7 @@ __global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
         if (lane != 0) return;
         TileIssuer<D, S> issuer;
         issuer.walk = walk;
+        issuer.start(p);
         bool done = false;
         while (!done)
             if (!issuer.issue_one(ring, full_bar, empty_bar, &tm_k, &tm_v, p, abort_flag, done)) break;

@@ -106,6 +106,28 @@ int gqa_decode_append(const void* q, const void* k_new, const void* v_new, void*
                       int B, int sq, int H, int G, int D, int Tmax, cudaStream_t stream);
 
 /*
+ * Decode step over a paged KV cache: the same attention as gqa_decode, with
+ * each sequence's cache held in fixed-size pages reached through a block table
+ * (the PagedAttention placement that "GQA analysis" names as orthogonal to GQA,
+ * sections "Tensor parallelism and kernel constraints" and "pros").
+ *
+ * k_pages, v_pages: [num_pages, G, page_size, D] bf16, device, 16-byte aligned:
+ *   page p holds page_size consecutive tokens of one sequence for every KV
+ *   head, each head's rows contiguous.
+ * block_table: [B, max_pages_per_seq] int32, device: entry (b, j) is the page
+ *   holding tokens [j*page_size, (j+1)*page_size) of sequence b. Only entries
+ *   for pages that start before seq_lens[b] are read; an entry outside
+ *   [0, num_pages) reads as zeros (no fault).
+ * page_size: a power of two, 8 <= page_size <= 65536. The cache capacity per
+ *   sequence is Tmax = max_pages_per_seq * page_size; seq_lens are clamped to it.
+ * Library-owned workspace, as for gqa_decode.
+ */
+int gqa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                     const int32_t* block_table, const int32_t* seq_lens, float scale, void* out,
+                     float* lse, int B, int sq, int H, int G, int D, int page_size, int num_pages,
+                     int max_pages_per_seq, cudaStream_t stream);
+
+/*
  * Bytes of device workspace gqa_decode_ex needs for these sizes on the current
  * device: two partial-result slots (O[R][D], running max m[R], sum l[R]) per
  * split-KV CTA plus the per-sequence tile prefix sums. Returns 0 for

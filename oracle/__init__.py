@@ -126,6 +126,30 @@ def gqa_decode_append_f64(q, k_cache, v_cache, k_new, v_new, seq_lens, scale, th
     return out, lse, k, v
 
 
+def gather_pages(k_pages, block_table, seq_lens, Tmax):
+    """The logical [B, G, Tmax, D] cache behind a paged one (PagedAttention's
+    placement, which "GQA analysis" names as orthogonal to GQA): token t of
+    sequence b lives in page block_table[b, t // page_size] at row
+    t % page_size. Only tokens before seq_lens[b] are gathered; the rest of
+    the logical cache is NaN (never read by the definition)."""
+    num_pages, G, ps, D = k_pages.shape
+    B = block_table.shape[0]
+    out = np.full((B, G, Tmax, D), 0x7FC0, dtype=np.uint16)
+    for b in range(B):
+        for t in range(min(int(seq_lens[b]), Tmax)):
+            out[b, :, t, :] = k_pages[int(block_table[b, t // ps]), :, t % ps, :]
+    return out
+
+
+def gqa_decode_paged_f64(q, k_pages, v_pages, block_table, seq_lens, scale, threads: int = 1):
+    """The decode definition over the logical caches a paged cache holds."""
+    ps = k_pages.shape[2]
+    Tmax = block_table.shape[1] * ps
+    k = gather_pages(k_pages, block_table, seq_lens, Tmax)
+    v = gather_pages(v_pages, block_table, seq_lens, Tmax)
+    return get().gqa_decode(q, k, v, seq_lens, scale, threads=threads)
+
+
 def get() -> Oracle:
     """The oracle built from gqa_oracle.c (compiled on first use)."""
     global _default

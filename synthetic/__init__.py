@@ -156,3 +156,37 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
     r[nan] = BF16_NAN
     return r
+
+
+def paginate(k: np.ndarray, v: np.ndarray, seq_lens: np.ndarray, page_size: int, seed: int,
+             spare_pages: int = 3, fill_bits: int = BF16_NAN):
+    """Lays contiguous caches [B, G, Tmax, D] out as pages [num_pages, G,
+    page_size, D] in a seeded random physical order. Every page that holds a
+    token before a sequence's length is placed; the spare pages and the
+    unused block-table entries point at NaN-filled pages, whose contents a
+    step must never let into its result. Returns (k_pages, v_pages,
+    block_table [B, max_pages] int32)."""
+    B, G, Tmax, D = k.shape
+    max_pages = -(-Tmax // page_size)
+    lens = np.clip(np.asarray(seq_lens, dtype=np.int64), 0, Tmax)
+    need = [int(-(-int(t) // page_size)) for t in lens]
+    num_pages = sum(need) + spare_pages
+    order = np.argsort(uniform_int(seed, 21, num_pages, 0, 2**31 - 1), kind="stable")
+    kp = np.full((num_pages, G, page_size, D), fill_bits, dtype=np.uint16)
+    vp = np.full((num_pages, G, page_size, D), fill_bits, dtype=np.uint16)
+    table = np.empty((B, max_pages), dtype=np.int32)
+    spare = [int(x) for x in order[sum(need):]] or [0]
+    nxt = 0
+    for b in range(B):
+        for j in range(max_pages):
+            if j < need[b]:
+                phys = int(order[nxt])
+                nxt += 1
+                rows = slice(j * page_size, min((j + 1) * page_size, Tmax))
+                n = rows.stop - rows.start
+                kp[phys, :, :n] = k[b, :, rows]
+                vp[phys, :, :n] = v[b, :, rows]
+                table[b, j] = phys
+            else:
+                table[b, j] = spare[(b + j) % len(spare)]
+    return kp, vp, table
