@@ -106,14 +106,16 @@ int check_shapes(int B, int sq, int H, int G, int D, int Tmax) {
     return GQA_OK;
 }
 
-// Smallest share of tiles worth giving a CTA. The default (4 tiles, 256
-// tokens) keeps small problems from being cut into one-tile partials; the
+// Smallest share of tiles worth giving a CTA. The default (16 tiles, 1024
+// tokens, a few microseconds of streaming) keeps small problems from being
+// cut into partials whose merge costs more than it saves (the 32 x 1024
+// tiny workload: 9 us unsplit against 12 us in four-way splits); the
 // environment variable exists for sweeps of the plan and for tests that want
 // many splits on small inputs.
 int min_tiles_per_cta() {
     const char* s = std::getenv("GQA_DECODE_MIN_TILES_PER_CTA");
     const int x = s ? std::atoi(s) : 0;
-    return x > 0 ? x : 4;
+    return x > 0 ? x : 16;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -336,7 +338,7 @@ int gqa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                      const int32_t* block_table, const int32_t* seq_lens, float scale, void* out,
                      float* lse, int B, int sq, int H, int G, int D, int page_size, int num_pages,
                      int max_pages_per_seq, cudaStream_t stream) {
-    if (page_size < 8 || page_size > 65536 || (page_size & (page_size - 1)) || num_pages <= 0 ||
+    if (page_size < 16 || page_size > 65536 || (page_size & (page_size - 1)) || num_pages <= 0 ||
         max_pages_per_seq <= 0)
         return page_size <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 ? GQA_ERR_INVALID_ARG
                                                                            : GQA_ERR_UNSUPPORTED;

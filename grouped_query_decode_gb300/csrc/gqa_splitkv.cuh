@@ -164,8 +164,10 @@ struct TileIssuer {
             if (p.page_size >= kTileTokens) {
                 r.page[0] = __ldg(bt + tok0 / p.page_size);
             } else {
-                for (int j = 0; j < kTileTokens / p.page_size; ++j)
-                    if (tok0 + j * p.page_size < r.tb) r.page[j] = __ldg(bt + tok0 / p.page_size + j);
+                const int n = kTileTokens / p.page_size;   // 2 or 4 pages of 32 or 16 tokens
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (j < n && tok0 + j * p.page_size < r.tb) r.page[j] = __ldg(bt + tok0 / p.page_size + j);
             }
         }
         return true;
@@ -183,13 +185,22 @@ struct TileIssuer {
             return true;
         }
         const TileRef r = cur;
-        have_cur = next(p, cur);
         const uint32_t it = issued;
         const int s = it % S;
         if (!wait_phase(empty_bar + 8 * s, ((it / S) & 1) ^ 1, abort_flag, p.status, p.wait_timeout_ns))
             return false;
         issued = it + 1;
-        if (blockIdx.x == 0 && (int)it == p.skip_tile) return true;  // injected fault
+        issue_copies(r, s, ring, full_bar, tm_k, tm_v, p, it);
+        // Look the next tile up now: its block-table reads are in flight
+        // while the producer waits for the next free stage.
+        have_cur = next(p, cur);
+        return true;
+    }
+
+    __device__ void issue_copies(const TileRef& r, int s, uint32_t ring, uint32_t full_bar,
+                                 const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                 const DecodeParams& p, uint32_t it) {
+        if (blockIdx.x == 0 && (int)it == p.skip_tile) return;  // injected fault
         constexpr int kStageBytes = 2 * kTileTokens * D * 2;
         constexpr int kTileBytes = kTileTokens * D * 2;
         constexpr int NB = D / kBoxCols;
@@ -220,9 +231,11 @@ struct TileIssuer {
             // zeroed in V), so the pages after the last one are not read.
             const int ps = p.page_size;
             int npages = 0;
-            for (int j = 0; j < kTileTokens / ps; ++j) npages += r.page[j] >= 0 ? 1 : 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) npages += r.page[j] >= 0 ? 1 : 0;
             mbar_arrive_expect_tx(fb, (uint32_t)npages * NB * ps * 128 * 2);
-            for (int j = 0; j < kTileTokens / ps; ++j) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
                 if (r.page[j] < 0) continue;
                 const int z = r.page[j] * p.G + r.g;
 #pragma unroll
@@ -233,7 +246,6 @@ struct TileIssuer {
                 }
             }
         }
-        return true;
     }
 
     // Waits (bounded) until the copies of tiles [consumed, issued) have landed,
@@ -305,30 +317,42 @@ __global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
     // tiles are shared by fewer CTAs if a grid that keeps at least 80% of
     // them busy lines up with the units: a whole number of units per CTA (no
     // unit split, nothing to merge), or, with fewer units than CTAs, the same
-    // whole number of CTAs per unit (every CTA one equal partial). The CTAs
-    // left over exit.
+    // whole number of CTAs per unit (every CTA one equal partial) on about 85%
+    // of the grid. The CTAs left over exit.
     if (warp == 0) {
-        constexpr int kCached = 8;
+        constexpr int kCached = 8;       // sequences 0..255 stay in registers
         long long cached[kCached];
         long long total = 0;
         int nt_min = 0x7fffffff, nt_max = 0;
-        for (int b0 = 0, k = 0; b0 < p.B; b0 += 32, ++k) {
-            const int b = b0 + lane;
-            const int nt = b < p.B ? (int)tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Tmax)) : 0;
-            if (b < p.B) {
-                nt_min = min(nt_min, nt);
-                nt_max = max(nt_max, nt);
-            }
-            const long long v = (long long)nt * p.G;
-            if (k < kCached) cached[k] = v;
+        auto tiles_times_g = [&](int b) -> long long {
+            if (b >= p.B) return 0;
+            const int nt = (int)tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Tmax));
+            nt_min = min(nt_min, nt);
+            nt_max = max(nt_max, nt);
+            return (long long)nt * p.G;
+        };
+        auto scan_add = [&](long long v) {
             long long incl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const long long n = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += n;
             }
-            total += __shfl_sync(0xffffffffu, incl, 31);
+            return incl;
+        };
+#pragma unroll
+        for (int k = 0; k < kCached; ++k) {
+            cached[k] = 0;
+            if (k * 32 < p.B) {
+                cached[k] = tiles_times_g(k * 32 + lane);
+                long long sum = cached[k];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                total += sum;
+            }
         }
+        for (int b0 = kCached * 32; b0 < p.B; b0 += 32)
+            total += __shfl_sync(0xffffffffu, scan_add(tiles_times_g(b0 + lane)), 31);
         nt_min = __reduce_min_sync(0xffffffffu, nt_min);
         nt_max = __reduce_max_sync(0xffffffffu, nt_max);
         long long P = p.ctas;
@@ -339,37 +363,35 @@ __global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
                 const long long even = (units + per - 1) / per;
                 if (units % per == 0 && 5 * even >= 4 * P) P = even;
             } else {
-                const long long even = units * (P / units);
-                if (5 * even >= 4 * P) P = even;
+                // Measured on the long-context and MQA-end workloads: about
+                // 85% of the SMs, each unit split evenly, beats every SM with
+                // uneven splits (fewer partials, HBM still saturated).
+                const long long even = units * ((P * 85 / 100) / units);
+                if (even >= units && 5 * even >= 4 * P) P = even;
             }
         }
+        // First sequence whose tiles reach past lo, and the tiles before it.
         const long long lo = (long long)blockIdx.x * total / P;
         long long pre = 0;
         int bstart = p.B;
         long long prestart = total;
-        for (int b0 = 0, k = 0; b0 < p.B && (long long)blockIdx.x < P; b0 += 32, ++k) {
-            const int b = b0 + lane;
-            long long v;
-            if (k < kCached) {
-                v = cached[k];
-            } else {
-                v = b < p.B ? tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Tmax)) * p.G : 0;
-            }
-            long long incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const long long n = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += n;
-            }
-            const unsigned hit = __ballot_sync(0xffffffffu, b < p.B && pre + incl > lo);
+        bool found = (long long)blockIdx.x >= P;
+        auto find = [&](int b0, long long v) {
+            const long long incl = scan_add(v);
+            const unsigned hit = __ballot_sync(0xffffffffu, b0 + lane < p.B && pre + incl > lo);
             if (hit) {
                 const int src = __ffs(hit) - 1;
                 bstart = b0 + src;
                 prestart = pre + __shfl_sync(0xffffffffu, incl - v, src);
-                break;
+                found = true;
+            } else {
+                pre += __shfl_sync(0xffffffffu, incl, 31);
             }
-            pre += __shfl_sync(0xffffffffu, incl, 31);
-        }
+        };
+#pragma unroll
+        for (int k = 0; k < kCached; ++k)
+            if (!found && k * 32 < p.B) find(k * 32, cached[k]);
+        for (int b0 = kCached * 32; !found && b0 < p.B; b0 += 32) find(b0, tiles_times_g(b0 + lane));
         if (lane == 0) {
             shared_ll[0] = total;
             shared_ll[1] = bstart;

@@ -118,7 +118,7 @@ int gqa_decode_append(const void* q, const void* k_new, const void* v_new, void*
  *   holding tokens [j*page_size, (j+1)*page_size) of sequence b. Only entries
  *   for pages that start before seq_lens[b] are read; an entry outside
  *   [0, num_pages) reads as zeros (no fault).
- * page_size: a power of two, 8 <= page_size <= 65536. The cache capacity per
+ * page_size: a power of two, 16 <= page_size <= 65536. The cache capacity per
  *   sequence is Tmax = max_pages_per_seq * page_size; seq_lens are clamped to it.
  * Library-owned workspace, as for gqa_decode.
  */

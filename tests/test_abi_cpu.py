@@ -47,9 +47,9 @@ def test_plan_shapes():
     # MQA end: 32 rows -> two 16-row tiles: 8 consumer warps + 1 producer warp.
     p = gq.gqa_decode_plan(64, 1, 32, 1, 128, 8192, 152)
     assert p["row_tiles"] == 2 and p["threads"] == 288
-    # A tiny problem gets at least 4 tiles per CTA.
+    # A tiny problem gets at least 16 tiles (1024 tokens) per CTA.
     p = gq.gqa_decode_plan(1, 1, 32, 8, 64, 1024, 152)
-    assert p["max_tiles"] == 128 and p["ctas"] == 32
+    assert p["max_tiles"] == 128 and p["ctas"] == 8
 
 
 def test_plan_min_tiles_override(monkeypatch):

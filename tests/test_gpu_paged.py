@@ -50,7 +50,7 @@ def test_paged_rejects_bad_page_sizes():
     out = torch.empty(1, 1, 8, 64, dtype=torch.bfloat16, device="cuda")
     dl, dt = torch.from_numpy(lens).cuda(), torch.from_numpy(table).cuda()
     lib = gq.load()
-    for ps, code in ((12, gq.GQA_ERR_UNSUPPORTED), (4, gq.GQA_ERR_UNSUPPORTED), (0, gq.GQA_ERR_INVALID_ARG)):
+    for ps, code in ((12, gq.GQA_ERR_UNSUPPORTED), (8, gq.GQA_ERR_UNSUPPORTED), (0, gq.GQA_ERR_INVALID_ARG)):
         rc = lib.gqa_decode_paged(dq.data_ptr(), dkp.data_ptr(), dvp.data_ptr(), dt.data_ptr(),
                                   dl.data_ptr(), 0.1, out.data_ptr(), None, 1, 1, 8, 2, 64, ps,
                                   kp.shape[0], table.shape[1], None)
