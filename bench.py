@@ -230,8 +230,9 @@ def run_reference(args, cfg):
     return 0
 
 
-def _config_dict(cfg, lens, l2_note, append=False, paged=0):
-    return {"workload": cfg.name + ("+append" if append else "") + (f"+paged{paged}" if paged else ""), "B": cfg.B, "sq": cfg.sq, "H": cfg.H, "G": cfg.G, "D": cfg.D,
+def _config_dict(cfg, lens, l2_note, append=False, paged=0, fp8=False):
+    return {"workload": cfg.name + ("+append" if append else "") + (f"+paged{paged}" if paged else "")
+            + ("+fp8" if fp8 else ""), "B": cfg.B, "sq": cfg.sq, "H": cfg.H, "G": cfg.G, "D": cfg.D,
             "Tmax": cfg.Tmax, "sum_T": int(np.sum(lens)), "scale": cfg.scale, "seed": cfg.seed,
             "inputs": "Q,K,V i.i.d. N(0,1) rounded to bf16", "l2": l2_note}
 
@@ -275,6 +276,19 @@ def run_gpu(args, cfg):
         dvn = to_dev(syn.normal_bf16(cfg.seed, 12, (cfg.B, cfg.sq, cfg.G, cfg.D)))
         nbytes += 2 * 2 * (cfg.B * cfg.sq * cfg.G * cfg.D * 2)   # new rows read + written
 
+    if args.fp8:
+        # The same caches as e4m3 codes with one fp32 scale per 64-token block.
+        kc, ksc = syn.fp8_cache(k, lens, tail_code=0)
+        vc, vsc = syn.fp8_cache(v, lens, tail_code=0)
+        fp8_sets = [(torch.from_numpy(kc).to(dev), torch.from_numpy(vc).to(dev),
+                     torch.from_numpy(ksc).to(dev), torch.from_numpy(vsc).to(dev))
+                    for _ in range(copies)]
+        host_fp8 = (kc, vc, ksc, vsc)
+        del dks[:], dvs[:]
+        nbytes -= kv_bytes(cfg.G, cfg.D, lens)                        # bf16 K/V ...
+        nbytes += kv_bytes(cfg.G, cfg.D, lens, elem_bytes=1)          # ... are 1-byte codes
+        nbytes += 2 * 4 * int(sum(-(-int(t) // 64) for t in lens)) * cfg.G   # block scales read
+
     if args.paged:
         # The same logical caches laid out in pages, one paged copy per
         # rotation slot, each with its own block table.
@@ -290,7 +304,10 @@ def run_gpu(args, cfg):
 
     def step(i):
         c = i % copies
-        if args.paged:
+        if args.fp8:
+            kc_, vc_, ks_, vs_ = fp8_sets[c]
+            gq.gqa_decode_fp8(dq, kc_, vc_, ks_, vs_, dl, cfg.scale, out, lse, stream=stream)
+        elif args.paged:
             kp_, vp_, tb_ = paged[c]
             gq.gqa_decode_paged(dq, kp_, vp_, tb_, dl, cfg.scale, out, lse, stream=stream)
         elif args.append:
@@ -357,7 +374,13 @@ def run_gpu(args, cfg):
 
     # End to end: inputs from pinned host memory, outputs back, every step.
     hq = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).pin_memory()
-    if args.paged:
+    if args.fp8:
+        hk = torch.from_numpy(host_fp8[0]).pin_memory()
+        hv = torch.from_numpy(host_fp8[1]).pin_memory()
+        hks = torch.from_numpy(host_fp8[2]).pin_memory()
+        hvs = torch.from_numpy(host_fp8[3]).pin_memory()
+        e2e_k, e2e_v, e2e_ks, e2e_vs = fp8_sets[0]
+    elif args.paged:
         hk = torch.from_numpy(host_paged[0].view(np.int16)).view(torch.bfloat16).pin_memory()
         hv = torch.from_numpy(host_paged[1].view(np.int16)).view(torch.bfloat16).pin_memory()
         htab = torch.from_numpy(host_paged[2]).pin_memory()
@@ -380,7 +403,11 @@ def run_gpu(args, cfg):
         e2e_k.copy_(hk, non_blocking=True)
         e2e_v.copy_(hv, non_blocking=True)
         dl.copy_(hl, non_blocking=True)
-        if args.paged:
+        if args.fp8:
+            e2e_ks.copy_(hks, non_blocking=True)
+            e2e_vs.copy_(hvs, non_blocking=True)
+            gq.gqa_decode_fp8(dq, e2e_k, e2e_v, e2e_ks, e2e_vs, dl, cfg.scale, out, lse, stream=stream)
+        elif args.paged:
             e2e_t.copy_(htab, non_blocking=True)
             gq.gqa_decode_paged(dq, e2e_k, e2e_v, e2e_t, dl, cfg.scale, out, lse, stream=stream)
         elif args.append:
@@ -404,6 +431,8 @@ def run_gpu(args, cfg):
     torch.cuda.synchronize(dev)
     e2e_ms, e2e_value = aggregate_over_ranks(a.elapsed_time(b) / e2e_steps, nbytes, device=dev)
     h2d = hq.nbytes + hk.nbytes + hv.nbytes + hl.nbytes + (htab.nbytes if args.paged else 0)
+    if args.fp8:
+        h2d += hks.nbytes + hvs.nbytes
     if args.append:
         h2d += hkn.nbytes + hvn.nbytes
     d2h = ho.nbytes + hlse.nbytes
@@ -422,7 +451,7 @@ def run_gpu(args, cfg):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "us_per_step": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": _config_dict(cfg, lens, append=args.append, paged=args.paged,
+            "config": _config_dict(cfg, lens, append=args.append, paged=args.paged, fp8=args.fp8,
                                    l2_note=f"inputs larger than L2: {copies} rotating "
                                                        f"K/V copies of {cache_bytes >> 20} MiB vs "
                                                        f"{l2 >> 20} MiB L2"),
@@ -464,6 +493,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--paged", type=int, default=0, metavar="PAGE_SIZE",
                     help="time gqa_decode_paged on the same caches split into pages of this size")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time gqa_decode_fp8 on the same caches as e4m3 codes with block scales")
     ap.add_argument("--append", action="store_true",
                     help="time gqa_decode_append (new K/V rows written in the same launch)")
     args = ap.parse_args(argv)

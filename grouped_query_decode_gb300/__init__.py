@@ -66,6 +66,8 @@ def load():
             lib.gqa_decode_append.restype = i32
             lib.gqa_decode_paged.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, *([i32] * 8), vp]
             lib.gqa_decode_paged.restype = i32
+            lib.gqa_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, vp, *shape, vp]
+            lib.gqa_decode_fp8.restype = i32
             lib.gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, f32, vp, vp, *shape, vp]
             lib.gqa_decode_noalloc.restype = i32
             lib.gqa_decode_workspace_bytes.argtypes = shape
@@ -185,6 +187,37 @@ def gqa_decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale, out, lse
                                  _stream_handle(stream, q.device))
     if rc != GQA_OK:
         raise GQADecodeError(rc, "gqa_decode_paged")
+
+
+def gqa_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, seq_lens, scale, out, lse=None,
+                   stream=None):
+    """One decode step over an fp8 cache: k_codes/v_codes [B, G, Tmax, 128]
+    uint8 e4m3 codes, k_scale/v_scale [B, G, ceil(Tmax/64)] float32 (one scale
+    per 64-token block)."""
+    import torch
+    for name, t, dt in (("q", q, torch.bfloat16), ("k_codes", k_codes, torch.uint8),
+                        ("v_codes", v_codes, torch.uint8), ("k_scale", k_scale, torch.float32),
+                        ("v_scale", v_scale, torch.float32), ("seq_lens", seq_lens, torch.int32),
+                        ("out", out, torch.bfloat16)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous {dt} CUDA tensor")
+    B, sq, H, D = q.shape
+    Bk, G, Tmax, Dk = k_codes.shape
+    if (Bk, Dk) != (B, D) or tuple(v_codes.shape) != tuple(k_codes.shape):
+        raise ValueError("k_codes / v_codes must be [B, G, Tmax, D]")
+    nt = (Tmax + 63) // 64
+    if tuple(k_scale.shape) != (B, G, nt) or tuple(v_scale.shape) != (B, G, nt):
+        raise ValueError("k_scale / v_scale must be [B, G, ceil(Tmax/64)]")
+    if tuple(seq_lens.shape) != (B,) or tuple(out.shape) != (B, sq, H, D):
+        raise ValueError("seq_lens must be [B] and out [B, sq, H, D]")
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, sq, H)):
+        raise ValueError("lse must be float32 [B, sq, H]")
+    rc = load().gqa_decode_fp8(q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(),
+                               k_scale.data_ptr(), v_scale.data_ptr(), seq_lens.data_ptr(),
+                               float(scale), out.data_ptr(), None if lse is None else lse.data_ptr(),
+                               B, sq, H, G, D, Tmax, _stream_handle(stream, q.device))
+    if rc != GQA_OK:
+        raise GQADecodeError(rc, "gqa_decode_fp8")
 
 
 def gqa_decode_ex(q, k_cache, v_cache, seq_lens, scale, out, lse, workspace, stream=None):

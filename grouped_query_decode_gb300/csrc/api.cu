@@ -80,16 +80,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // tensor; boxes of box_rows rows x 64 elements (128 bytes) with the 128-byte
 // swizzle. Reads past a slab's rows, or of a slab out of range, give 0.
 int encode_cache_map(CUtensorMap* map, const void* base, long long slabs, int rows, int D,
-                     int box_rows) {
+                     int box_rows, int elem_bytes = 2) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return cuda_fail(cudaErrorNotSupported);
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)slabs};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows * D * 2};
-    cuuint32_t box[3] = {(cuuint32_t)kBoxCols, (cuuint32_t)box_rows, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)D * elem_bytes, (cuuint64_t)rows * D * elem_bytes};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes), (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(map, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
     return GQA_OK;
 }
@@ -200,10 +201,16 @@ struct Paging {
     int page_size = 0, num_pages = 0, max_pages = 0;
 };
 
+struct Fp8Scales {
+    const float* k_scale = nullptr;        // null: bf16 cache
+    const float* v_scale = nullptr;
+};
+
 int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
             float scale, void* out, float* lse, int B, int sq, int H, int G, int D, int Tmax,
             void* workspace, size_t workspace_bytes, cudaStream_t stream, const void* k_new,
-            const void* v_new, const Paging& pg = Paging()) {
+            const void* v_new, const Paging& pg = Paging(), const Fp8Scales& f8 = Fp8Scales()) {
+    const bool kv8 = f8.k_scale != nullptr;
     if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_INVALID_ARG;
     int st = check_shapes(B, sq, H, G, D, Tmax);
     if (st != GQA_OK) return st;
@@ -226,9 +233,9 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32
     const long long slabs = pg.block_table ? (long long)pg.num_pages * G : (long long)B * G;
     const int rows = pg.block_table ? pg.page_size : Tmax;
     const int box_rows = pg.block_table && pg.page_size < kTileTokens ? pg.page_size : kTileTokens;
-    st = encode_cache_map(&a.tm_k, k_cache, slabs, rows, D, box_rows);
+    st = encode_cache_map(&a.tm_k, k_cache, slabs, rows, D, box_rows, kv8 ? 1 : 2);
     if (st != GQA_OK) return st;
-    st = encode_cache_map(&a.tm_v, v_cache, slabs, rows, D, box_rows);
+    st = encode_cache_map(&a.tm_v, v_cache, slabs, rows, D, box_rows, kv8 ? 1 : 2);
     if (st != GQA_OK) return st;
     a.p.q = static_cast<const uint16_t*>(q);
     a.p.seq_lens = seq_lens;
@@ -256,10 +263,14 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32
     a.p.block_table = pg.block_table;
     a.p.page_size = pg.page_size;
     a.p.max_pages = pg.max_pages;
+    a.p.k_scale = f8.k_scale;
+    a.p.v_scale = f8.v_scale;
+    a.p.scale_tiles = (Tmax + kTileTokens - 1) / kTileTokens;
+    a.kv8 = kv8;
     a.row_tiles = plan.row_tiles;
     a.pdl = true;
     a.stream = stream;
-    cudaError_t e = D == 64 ? launch_d64(a) : launch_d128(a);
+    cudaError_t e = kv8 ? launch_d128_fp8(a) : (D == 64 ? launch_d64(a) : launch_d128(a));
     if (e != cudaSuccess) return cuda_fail(e);
     return GQA_OK;
 }
@@ -364,6 +375,29 @@ int gqa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                    stream, nullptr, nullptr, pg);
 }
 
+int gqa_decode_fp8(const void* q, const void* k_codes, const void* v_codes, const float* k_scale,
+                   const float* v_scale, const int32_t* seq_lens, float scale, void* out, float* lse,
+                   int B, int sq, int H, int G, int D, int Tmax, cudaStream_t stream) {
+    int st = check_shapes(B, sq, H, G, D, Tmax);
+    if (st != GQA_OK) return st;
+    if (D != 128) return GQA_ERR_UNSUPPORTED;
+    if (!q || !k_codes || !v_codes || !k_scale || !v_scale || !seq_lens || !out)
+        return GQA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+        return GQA_ERR_MISALIGNED;
+    const size_t need = gqa_decode_workspace_bytes(B, sq, H, G, D, Tmax);
+    if (need == 0) return GQA_ERR_CUDA;
+    void* ws = nullptr;
+    size_t have = 0;
+    st = stream_workspace(stream, need, &ws, &have);
+    if (st != GQA_OK) return st;
+    Fp8Scales f8;
+    f8.k_scale = k_scale;
+    f8.v_scale = v_scale;
+    return enqueue(q, k_codes, v_codes, seq_lens, scale, out, lse, B, sq, H, G, D, Tmax, ws, have,
+                   stream, nullptr, nullptr, Paging(), f8);
+}
+
 int gqa_decode_check_error(cudaStream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -402,17 +436,18 @@ const char* gqa_decode_strerror(int status) {
 
 namespace gqa {
 
-int splitkv_smem_bytes(int D, int mt) {
-    if (D == 64) return mt == 1 ? KernelShape<64, 1>::kSmemBytes : KernelShape<64, 2>::kSmemBytes;
-    return mt == 1 ? KernelShape<128, 1>::kSmemBytes : KernelShape<128, 2>::kSmemBytes;
+template <template <int, int, bool> class F>
+int shape_query(int D, int mt, bool kv8) {
+    if (kv8) return mt == 1 ? F<128, 1, true>::value : F<128, 2, true>::value;
+    if (D == 64) return mt == 1 ? F<64, 1, false>::value : F<64, 2, false>::value;
+    return mt == 1 ? F<128, 1, false>::value : F<128, 2, false>::value;
 }
-int splitkv_threads(int D, int mt) {
-    if (D == 64) return mt == 1 ? KernelShape<64, 1>::kThreads : KernelShape<64, 2>::kThreads;
-    return mt == 1 ? KernelShape<128, 1>::kThreads : KernelShape<128, 2>::kThreads;
-}
-int splitkv_stages(int D, int mt) {
-    if (D == 64) return mt == 1 ? KernelShape<64, 1>::kStages : KernelShape<64, 2>::kStages;
-    return mt == 1 ? KernelShape<128, 1>::kStages : KernelShape<128, 2>::kStages;
-}
+template <int D, int MT, bool KV8> struct SmemQ { static constexpr int value = KernelShape<D, MT, KV8>::kSmemBytes; };
+template <int D, int MT, bool KV8> struct ThrQ { static constexpr int value = KernelShape<D, MT, KV8>::kThreads; };
+template <int D, int MT, bool KV8> struct StgQ { static constexpr int value = KernelShape<D, MT, KV8>::kStages; };
+
+int splitkv_smem_bytes(int D, int mt, bool kv8) { return shape_query<SmemQ>(D, mt, kv8); }
+int splitkv_threads(int D, int mt, bool kv8) { return shape_query<ThrQ>(D, mt, kv8); }
+int splitkv_stages(int D, int mt, bool kv8) { return shape_query<StgQ>(D, mt, kv8); }
 
 }  // namespace gqa

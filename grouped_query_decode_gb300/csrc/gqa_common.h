@@ -62,6 +62,11 @@ struct DecodeParams {
     // page j of sequence b to its physical page.
     const int32_t* block_table;
     int page_size, max_pages;
+    // fp8 caches (KV8 kernels): per (unit, 64-token tile) dequantisation
+    // scales, [B*G][scale_tiles] fp32; element value = e4m3 code * scale.
+    const float* k_scale;
+    const float* v_scale;
+    int scale_tiles;
 };
 
 // One CTA per SM. Every 16-row tile of the group has four consumer warps
@@ -69,7 +74,7 @@ struct DecodeParams {
 // the TMA copies. With two row tiles (9 warps, which the register file
 // allocates as 12) a thread gets 168 registers, so those warps keep their Q
 // fragments in shared memory rather than in registers.
-template <int D, int MT>
+template <int D, int MT, bool KV8 = false>
 struct KernelShape {
     static constexpr int kConsumerWarps = kSlices * MT;
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;
@@ -80,9 +85,14 @@ struct KernelShape {
         (65536 / (kAllocWarps * 32)) / 8 * 8 > 255 ? 255 : (65536 / (kAllocWarps * 32)) / 8 * 8;
     static constexpr bool kQInSmem = MT > 1;
     static constexpr int kQBytesPerWarp = kQInSmem ? 16 * D * 2 : 0;
-    static constexpr int kBoxes = D / kBoxCols;
-    static constexpr int kTileBytes = kTileTokens * D * 2;   // K (or V) of one stage
+    // K/V elements as stored in the cache: bf16, or fp8 e4m3 codes (KV8).
+    static constexpr int kElemBytes = KV8 ? 1 : 2;
+    static constexpr int kBoxElems = 128 / kElemBytes;        // elements per 128-byte box row
+    static constexpr int kBoxes = D / kBoxElems;
+    static constexpr int kTileBytes = kTileTokens * D * kElemBytes;   // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
+    // KV8: each consumer warp's fp16 copy of its 16 K and 16 V rows.
+    static constexpr int kStagingBytesPerWarp = KV8 ? 2 * 16 * D * 2 : 0;
     // Per row tile: the slice-merge buffer (3 slices x 16 x D floats), which
     // the cross-CTA merge reuses for a slot index, 16 maxima and 16 weights per
     // contributor.
@@ -92,11 +102,12 @@ struct KernelShape {
     static constexpr int kMergeBytes = MT * kMergeFloatsPerTile * 4;
     static constexpr int kMlBytes = MT * kSlices * 16 * 2 * 4;
     static constexpr int kQBytes = kConsumerWarps * kQBytesPerWarp;
-    static constexpr int kStages = D == 128 ? (MT == 1 ? 5 : 4) : 8;
+    static constexpr int kStagingBytes = kConsumerWarps * kStagingBytesPerWarp;
+    static constexpr int kStages = KV8 ? (MT == 1 ? 8 : 4) : (D == 128 ? (MT == 1 ? 5 : 4) : 8);
     static constexpr int kBarBytes = 8 * (2 * kStages + 4 * MT) + 64;
     // +1024 so the ring can be aligned to the 1 KB swizzle atom at run time.
-    static constexpr int kSmemBytes =
-        1024 + kStages * kStageBytes + kMergeBytes + kMlBytes + kQBytes + kBarBytes;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kMergeBytes + kMlBytes + kQBytes +
+                                      kStagingBytes + kBarBytes;
 };
 
 }  // namespace gqa

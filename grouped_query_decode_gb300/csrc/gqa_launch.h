@@ -14,6 +14,7 @@ struct LaunchArgs {
     CUtensorMap tm_v;
     DecodeParams p;
     int row_tiles;   // 1 or 2
+    bool kv8;        // fp8 e4m3 K/V codes with per-tile scales
     bool pdl;        // launch with programmatic stream serialization
     cudaStream_t stream;
 };
@@ -21,10 +22,11 @@ struct LaunchArgs {
 // Enqueue the split-KV kernel (one launch per decode step) for D = 64 / D = 128.
 cudaError_t launch_d64(const LaunchArgs& a);
 cudaError_t launch_d128(const LaunchArgs& a);
+cudaError_t launch_d128_fp8(const LaunchArgs& a);
 
 // Dynamic shared memory and threads per CTA of the split-KV kernel.
-int splitkv_smem_bytes(int D, int row_tiles);
-int splitkv_threads(int D, int row_tiles);
-int splitkv_stages(int D, int row_tiles);
+int splitkv_smem_bytes(int D, int row_tiles, bool kv8 = false);
+int splitkv_threads(int D, int row_tiles, bool kv8 = false);
+int splitkv_stages(int D, int row_tiles, bool kv8 = false);
 
 }  // namespace gqa

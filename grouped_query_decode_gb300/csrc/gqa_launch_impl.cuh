@@ -8,9 +8,9 @@
 
 namespace gqa {
 
-template <int D, int MT>
+template <int D, int MT, bool KV8>
 cudaError_t launch_splitkv(const LaunchArgs& a) {
-    using KS = KernelShape<D, MT>;
+    using KS = KernelShape<D, MT, KV8>;
     // The shared-memory opt-in is per function and per device.
     static std::atomic<unsigned long long> attr_set_mask{0};
     int dev = 0;
@@ -18,7 +18,7 @@ cudaError_t launch_splitkv(const LaunchArgs& a) {
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(attr_set_mask.load() & bit)) {
-        e = cudaFuncSetAttribute(gqa_splitkv_kernel<D, MT>,
+        e = cudaFuncSetAttribute(gqa_splitkv_kernel<D, MT, KV8>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, KS::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set_mask.fetch_or(bit);
@@ -34,7 +34,7 @@ cudaError_t launch_splitkv(const LaunchArgs& a) {
     cfg.stream = a.stream;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gqa_splitkv_kernel<D, MT>, a.tm_k, a.tm_v, a.p);
+    return cudaLaunchKernelEx(&cfg, gqa_splitkv_kernel<D, MT, KV8>, a.tm_k, a.tm_v, a.p);
 }
 
 }  // namespace gqa

@@ -136,7 +136,7 @@ struct TileRef {
 // consumers are done with the tile S places earlier. The next tile is looked
 // up one step ahead, so that its block-table reads (paged caches) are in
 // flight while the producer waits for a free stage.
-template <int D, int S>
+template <int D, int S, bool KV8>
 struct TileIssuer {
     SegmentWalker walk;
     Segment sg;
@@ -201,9 +201,11 @@ struct TileIssuer {
                                  const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                  const DecodeParams& p, uint32_t it) {
         if (blockIdx.x == 0 && (int)it == p.skip_tile) return;  // injected fault
-        constexpr int kStageBytes = 2 * kTileTokens * D * 2;
-        constexpr int kTileBytes = kTileTokens * D * 2;
-        constexpr int NB = D / kBoxCols;
+        using KS = KernelShape<D, 1, KV8>;
+        constexpr int kStageBytes = KS::kStageBytes;
+        constexpr int kTileBytes = KS::kTileBytes;
+        constexpr int NB = KS::kBoxes;
+        constexpr int kBoxCols = KS::kBoxElems;
         const uint32_t fb = full_bar + 8 * s;
         const uint32_t kdst = ring + s * kStageBytes;
         const uint32_t vdst = kdst + kTileBytes;
@@ -233,7 +235,7 @@ struct TileIssuer {
             int npages = 0;
 #pragma unroll
             for (int j = 0; j < 4; ++j) npages += r.page[j] >= 0 ? 1 : 0;
-            mbar_arrive_expect_tx(fb, (uint32_t)npages * NB * ps * 128 * 2);
+            mbar_arrive_expect_tx(fb, (uint32_t)npages * NB * ps * 128 * 2);  // paged: bf16 only
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 if (r.page[j] < 0) continue;
@@ -264,11 +266,11 @@ struct TileIssuer {
     }
 };
 
-template <int D, int MT>
-__global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
+template <int D, int MT, bool KV8>
+__global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     gqa_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
-    using KS = KernelShape<D, MT>;
+    using KS = KernelShape<D, MT, KV8>;
     constexpr int S = KS::kStages;
     constexpr int KSTEPS = D / 16;   // k16 steps of Q.K^T
     constexpr int NTILE_D = D / 8;   // n8 tiles of P.V (columns of O)
@@ -281,7 +283,8 @@ __global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
     float* merge_buf = reinterpret_cast<float*>(ring_ptr + S * KS::kStageBytes);
     float* ml_buf = merge_buf + KS::kMergeBytes / 4;
     unsigned char* q_smem = reinterpret_cast<unsigned char*>(ml_buf + KS::kMlBytes / 4);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(q_smem + KS::kQBytes);
+    unsigned char* staging = q_smem + KS::kQBytes;   // KV8 only; 512-byte aligned
+    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + KS::kStagingBytes);
     const uint32_t full_bar = smem_addr(bars);
     const uint32_t empty_bar = full_bar + 8 * S;
     const uint32_t merge_bar = empty_bar + 8 * S;          // [MT][4]: A, B, C, D
@@ -417,7 +420,7 @@ __global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
     if (is_producer) {
         // ------------------------------------------ dedicated producer warp
         if (lane != 0) return;
-        TileIssuer<D, S> issuer;
+        TileIssuer<D, S, KV8> issuer;
         issuer.walk = walk;
         issuer.start(p);
         bool done = false;
@@ -490,6 +493,10 @@ __global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
                     qa[kk][1] = q_hi ? __ldg(reinterpret_cast<const unsigned*>(q_hi + c)) : 0u;
                     qa[kk][2] = q_lo ? __ldg(reinterpret_cast<const unsigned*>(q_lo + c + 8)) : 0u;
                     qa[kk][3] = q_hi ? __ldg(reinterpret_cast<const unsigned*>(q_hi + c + 8)) : 0u;
+                    if constexpr (KV8) {   // fp16 MMAs: Q in fp16 (exact in fp16's range)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) qa[kk][e] = bf16x2_to_f16x2(qa[kk][e]);
+                    }
                 }
             } else {
                 // This warp's 16 Q rows into its own shared-memory copy, 16-byte
@@ -502,6 +509,12 @@ __global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
                         const int j = r / p.sq, sq_i = r % p.sq;
                         const int qrow = (sg.b * p.sq + sq_i) * p.H + sg.g * p.heads_per_group + j;
                         v = __ldg(reinterpret_cast<const uint4*>(p.q + (size_t)qrow * D) + chunk);
+                        if constexpr (KV8) {
+                            v.x = bf16x2_to_f16x2(v.x);
+                            v.y = bf16x2_to_f16x2(v.y);
+                            v.z = bf16x2_to_f16x2(v.z);
+                            v.w = bf16x2_to_f16x2(v.w);
+                        }
                     }
                     *reinterpret_cast<uint4*>(q_smem + warp * KS::kQBytesPerWarp + row * (D * 2) +
                                               ((chunk ^ (row & 7)) << 4)) = v;
@@ -520,8 +533,24 @@ __global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
 #pragma unroll
         for (int n = 0; n < NTILE_D; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
+        // KV8: the dequantisation scales of this unit's tiles, read one tile
+        // ahead of use so that their latency hides behind the current tile.
+        const size_t scale_row = ((size_t)sg.b * p.G + sg.g) * p.scale_tiles;
+        float ks_next = 1.f, vs_next = 1.f;
+        if constexpr (KV8) {
+            ks_next = __ldg(p.k_scale + scale_row + sg.t0);
+            vs_next = __ldg(p.v_scale + scale_row + sg.t0);
+        }
+
         for (int i = 0; i < sg.ntiles; ++i, ++it) {
             const int s = it % S;
+            const float ks = ks_next, vs = vs_next;
+            if constexpr (KV8) {
+                if (i + 1 < sg.ntiles) {
+                    ks_next = __ldg(p.k_scale + scale_row + sg.t0 + i + 1);
+                    vs_next = __ldg(p.v_scale + scale_row + sg.t0 + i + 1);
+                }
+            }
             if (!wait_phase(full_bar + 8 * s, (it / S) & 1, abort_flag, p.status, tmo)) {
                 failed = true;
                 break;
@@ -530,9 +559,50 @@ __global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
             const uint32_t vst = kst + KS::kTileBytes;
             const int tbase = (sg.t0 + i) * kTileTokens;
 
+            // KV8: this warp's 16 K and V rows, e4m3 codes, into its fp16
+            // staging copy (the same swizzled layout as a bf16 stage, 16 rows
+            // high); V rows past the valid length become 0. The fp8 stage is
+            // then released at once. Every e4m3 value is an fp16 value, so the
+            // copy is exact; the scales are applied to the scores and to P.
+            uint32_t k_src = kst, v_src = vst;
+            int k_row0 = slice * 16, box_stride = kTileTokens * 128;
+            if constexpr (KV8) {
+                const uint32_t stk = smem_addr(staging) + warp * KS::kStagingBytesPerWarp;
+                const uint32_t stv = stk + 16 * D * 2;
+                __syncwarp();   // this warp's previous reads of its staging are done
+                for (int u = lane; u < 2 * 16 * (D / 16); u += 32) {
+                    const int is_v = u >= 16 * (D / 16);
+                    const int uu = is_v ? u - 16 * (D / 16) : u;
+                    const int row = uu / (D / 16), c8 = uu % (D / 16);   // 16 codes per chunk
+                    const int srow = slice * 16 + row;
+                    const uint4 codes = ld_shared_v4((is_v ? vst : kst) + (c8 >> 3) * (kTileTokens * 128) +
+                                                     srow * 128 + (((c8 & 7) ^ (srow & 7)) << 4));
+                    uint4 h0, h1;
+                    if (is_v && tbase + srow >= sg.tb) {
+                        h0 = make_uint4(0u, 0u, 0u, 0u);
+                        h1 = h0;
+                    } else {
+                        h0 = make_uint4(e4m3x2_to_f16x2((uint16_t)codes.x), e4m3x2_to_f16x2((uint16_t)(codes.x >> 16)),
+                                        e4m3x2_to_f16x2((uint16_t)codes.y), e4m3x2_to_f16x2((uint16_t)(codes.y >> 16)));
+                        h1 = make_uint4(e4m3x2_to_f16x2((uint16_t)codes.z), e4m3x2_to_f16x2((uint16_t)(codes.z >> 16)),
+                                        e4m3x2_to_f16x2((uint16_t)codes.w), e4m3x2_to_f16x2((uint16_t)(codes.w >> 16)));
+                    }
+                    const int c16 = 2 * c8;                       // first fp16 chunk
+                    const uint32_t dst = (is_v ? stv : stk) + (c16 >> 3) * (16 * 128) + row * 128;
+                    st_shared_v4(dst + (((c16 & 7) ^ (row & 7)) << 4), h0);
+                    st_shared_v4(dst + ((((c16 + 1) & 7) ^ (row & 7)) << 4), h1);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar + 8 * s);
+                k_src = stk;
+                v_src = stv;
+                k_row0 = 0;
+                box_stride = 16 * 128;
+            }
+
             // Rows past the valid length may hold anything (NaN included);
             // zero them in V so that p = 0 times them stays 0.
-            if (tbase + kTileTokens > sg.tb) {
+            if (!KV8 && tbase + kTileTokens > sg.tb) {
                 bool wrote = false;
                 for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
                     const int row = slice * 16 + idx / (D / 8);
@@ -553,7 +623,7 @@ __global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
             // warp patches them into the stage before reading it and (one row
             // tile's warp) stores them to the cache. Each position lies in
             // exactly one tile, which one CTA owns, so no other CTA reads it.
-            if (p.k_new != nullptr) {
+            if (!KV8 && p.k_new != nullptr) {
                 const int new_lo = sg.tb - p.sq;
                 const int lo = max(new_lo, tbase + slice * 16);
                 const int hi = min(sg.tb, tbase + slice * 16 + 16);
@@ -583,24 +653,28 @@ __global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
 
             // S = Q K^T for this warp's 16 tokens: two n8 tiles.
             float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const int kt = k_tok - slice * 16 + k_row0;   // K row in the tile being read
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
                 const int chunk = kk * 2 + k_half;
                 const int bx = chunk >> 3, cc = chunk & 7;
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4(kst + bx * (kTileTokens * 128) + k_tok * 128 + ((cc ^ (k_tok & 7)) << 4), b0,
-                        b1, b2, b3);
+                ldsm_x4(k_src + bx * box_stride + kt * 128 + ((cc ^ (kt & 7)) << 4), b0, b1, b2, b3);
+                uint32_t a_s[4];
                 if constexpr (kQs) {
                     const int qc = kk * 2 + (lane >> 4);
-                    uint32_t a[4];
-                    ldsm_x4(qa_base + ((qc ^ (qa_row & 7)) << 4), a[0], a[1], a[2], a[3]);
+                    ldsm_x4(qa_base + ((qc ^ (qa_row & 7)) << 4), a_s[0], a_s[1], a_s[2], a_s[3]);
+                }
+                const uint32_t(&a)[4] = kQs ? a_s : qa[kQs ? 0 : kk];
+                if constexpr (KV8) {
+                    mma_f16_16816(sc[0], a, b0, b1);
+                    mma_f16_16816(sc[1], a, b2, b3);
+                } else {
                     mma_bf16_16816(sc[0], a, b0, b1);
                     mma_bf16_16816(sc[1], a, b2, b3);
-                } else {
-                    mma_bf16_16816(sc[0], qa[kk], b0, b1);
-                    mma_bf16_16816(sc[1], qa[kk], b2, b3);
                 }
             }
+            const float sscale = KV8 ? p.scale_log2 * ks : p.scale_log2;
 
             // Scale into the base-2 domain and mask invisible keys.
             float x[2][4];
@@ -608,16 +682,16 @@ __global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) x[j][c] = sc[j][c] * p.scale_log2;
+                    for (int c = 0; c < 4; ++c) x[j][c] = sc[j][c] * sscale;
             } else {
                 const int tok = tbase + slice * 16 + 2 * quad;
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int t = tok + 8 * j;
-                    x[j][0] = (t <= lim_lo) ? sc[j][0] * p.scale_log2 : -INFINITY;
-                    x[j][1] = (t + 1 <= lim_lo) ? sc[j][1] * p.scale_log2 : -INFINITY;
-                    x[j][2] = (t <= lim_hi) ? sc[j][2] * p.scale_log2 : -INFINITY;
-                    x[j][3] = (t + 1 <= lim_hi) ? sc[j][3] * p.scale_log2 : -INFINITY;
+                    x[j][0] = (t <= lim_lo) ? sc[j][0] * sscale : -INFINITY;
+                    x[j][1] = (t + 1 <= lim_lo) ? sc[j][1] * sscale : -INFINITY;
+                    x[j][2] = (t <= lim_hi) ? sc[j][2] * sscale : -INFINITY;
+                    x[j][3] = (t + 1 <= lim_hi) ? sc[j][3] * sscale : -INFINITY;
                 }
             }
             float mx_lo = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
@@ -664,22 +738,37 @@ __global__ void __maxnreg__((KernelShape<D, MT>::kMaxRegs))
 
             // The S accumulator layout is the A-operand layout of P.V.
             uint32_t pa[4];
-            pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
-            pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
-            pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
-            pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+            if constexpr (KV8) {
+                // P times the tile's V scale: O accumulates code-valued V.
+                pa[0] = pack_f16x2(pr[0][0] * vs, pr[0][1] * vs);
+                pa[1] = pack_f16x2(pr[0][2] * vs, pr[0][3] * vs);
+                pa[2] = pack_f16x2(pr[1][0] * vs, pr[1][1] * vs);
+                pa[3] = pack_f16x2(pr[1][2] * vs, pr[1][3] * vs);
+            } else {
+                pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+                pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+                pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+                pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+            }
+            const int vt = v_tok - slice * 16 + k_row0;   // V row in the tile being read
 #pragma unroll
             for (int n = 0; n < NTILE_D; n += 2) {
                 const int chunk = n + v_dt;
                 const int bx = chunk >> 3, cc = chunk & 7;
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(vst + bx * (kTileTokens * 128) + v_tok * 128 + ((cc ^ (v_tok & 7)) << 4),
-                              b0, b1, b2, b3);
-                mma_bf16_16816(o[n], pa, b0, b1);
-                mma_bf16_16816(o[n + 1], pa, b2, b3);
+                ldsm_x4_trans(v_src + bx * box_stride + vt * 128 + ((cc ^ (vt & 7)) << 4), b0, b1, b2, b3);
+                if constexpr (KV8) {
+                    mma_f16_16816(o[n], pa, b0, b1);
+                    mma_f16_16816(o[n + 1], pa, b2, b3);
+                } else {
+                    mma_bf16_16816(o[n], pa, b0, b1);
+                    mma_bf16_16816(o[n + 1], pa, b2, b3);
+                }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar + 8 * s);
+            if constexpr (!KV8) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar + 8 * s);
+            }
         }
         if (failed) break;
 

@@ -4,8 +4,8 @@
 namespace gqa {
 
 cudaError_t launch_d128(const LaunchArgs& a) {
-    return a.row_tiles == 1 ? launch_splitkv<128, 1>(a)
-                            : launch_splitkv<128, 2>(a);
+    return a.row_tiles == 1 ? launch_splitkv<128, 1, false>(a)
+                            : launch_splitkv<128, 2, false>(a);
 }
 
 }  // namespace gqa

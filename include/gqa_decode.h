@@ -128,6 +128,26 @@ int gqa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                      int max_pages_per_seq, cudaStream_t stream);
 
 /*
+ * Decode step over an fp8 KV cache: KV-cache quantisation, which "GQA
+ * analysis" names as orthogonal to GQA (element precision, with scale
+ * metadata; sections "KV cache" and "pros"). Each element is stored as an
+ * e4m3 code (OCP FP8 E4M3: 1 sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits, no infinities, S.1111.111 is NaN) and one fp32 scale covers a 64-token
+ * block of one (sequence, KV head): value = decode(code) * scale. Same
+ * attention and outputs as gqa_decode over the dequantised cache.
+ *
+ * k_codes, v_codes: [B, G, Tmax, D] uint8 e4m3 codes, device, 16-byte aligned.
+ * k_scale, v_scale: [B, G, ceil(Tmax / 64)] fp32, device; entry (b, g, j)
+ *   scales tokens [64 j, 64 j + 64) of KV head g of sequence b.
+ * D must be 128. The tensor-core products run in fp16 (every e4m3 value and
+ * the bf16 queries of ordinary magnitude, |q| < 65504, are exact in fp16).
+ * Library-owned workspace, as for gqa_decode.
+ */
+int gqa_decode_fp8(const void* q, const void* k_codes, const void* v_codes, const float* k_scale,
+                   const float* v_scale, const int32_t* seq_lens, float scale, void* out, float* lse,
+                   int B, int sq, int H, int G, int D, int Tmax, cudaStream_t stream);
+
+/*
  * Bytes of device workspace gqa_decode_ex needs for these sizes on the current
  * device: two partial-result slots (O[R][D], running max m[R], sum l[R]) per
  * split-KV CTA plus the per-sequence tile prefix sums. Returns 0 for

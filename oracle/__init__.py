@@ -56,8 +56,17 @@ class Oracle:
         lib.oracle_gqa_decode_f64.argtypes = [vp, vp, vp, vp, ctypes.c_double,
                                               i32, i32, i32, i32, i32, i32, lng, lng, vp, vp]
         lib.oracle_gqa_decode_f64.restype = ctypes.c_int
+        if hasattr(lib, "oracle_gqa_decode_kvf64"):
+            lib.oracle_gqa_decode_kvf64.argtypes = lib.oracle_gqa_decode_f64.argtypes
+            lib.oracle_gqa_decode_kvf64.restype = ctypes.c_int
         self._lib = lib
         self.path = lib_path
+
+    def gqa_decode_kv(self, q, k, v, seq_lens, scale, rows=None, threads: int = 1):
+        """As gqa_decode, with k and v given as float64 arrays."""
+        return self._run(self._lib.oracle_gqa_decode_kvf64, q,
+                         np.ascontiguousarray(k, dtype=np.float64),
+                         np.ascontiguousarray(v, dtype=np.float64), seq_lens, scale, rows, threads)
 
     def gqa_decode(self, q, k, v, seq_lens, scale, rows=None, threads: int = 1):
         """q [B,sq,H,D], k/v [B,G,Tmax,D] as bf16 bit arrays (uint16); seq_lens [B].
@@ -67,9 +76,11 @@ class Oracle:
         others are left NaN. `threads` splits the rows over host threads (each
         row is still computed by one thread in index order, so the result does
         not depend on the split)."""
+        return self._run(self._lib.oracle_gqa_decode_f64, q, np.ascontiguousarray(k, dtype=np.uint16),
+                         np.ascontiguousarray(v, dtype=np.uint16), seq_lens, scale, rows, threads)
+
+    def _run(self, fn, q, k, v, seq_lens, scale, rows, threads):
         q = np.ascontiguousarray(q, dtype=np.uint16)
-        k = np.ascontiguousarray(k, dtype=np.uint16)
-        v = np.ascontiguousarray(v, dtype=np.uint16)
         lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
         B, sq, H, D = q.shape
         Bk, G, Tmax, Dk = k.shape
@@ -83,7 +94,7 @@ class Oracle:
         bounds = [r0 + ((r1 - r0) * i) // threads for i in range(threads + 1)]
 
         def work(i):
-            return self._lib.oracle_gqa_decode_f64(
+            return fn(
                 q.ctypes.data, k.ctypes.data, v.ctypes.data, lens.ctypes.data, float(scale),
                 B, sq, H, G, D, Tmax, bounds[i], bounds[i + 1], out.ctypes.data, lse.ctypes.data)
 
@@ -148,6 +159,35 @@ def gqa_decode_paged_f64(q, k_pages, v_pages, block_table, seq_lens, scale, thre
     k = gather_pages(k_pages, block_table, seq_lens, Tmax)
     v = gather_pages(v_pages, block_table, seq_lens, Tmax)
     return get().gqa_decode(q, k, v, seq_lens, scale, threads=threads)
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """OCP FP8 E4M3 codes to their values: sign bit, 4 exponent bits with bias
+    7, 3 mantissa bits; exponent 0 is subnormal (m * 2^-9); no infinities, and
+    S.1111.111 is NaN."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = c & 7
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((e == 15) & (m == 7), np.nan, val)
+    return sign * val
+
+
+def dequantize_fp8(codes, scales) -> np.ndarray:
+    """The values of an fp8 cache: [B, G, Tmax, D] codes times the scale of
+    their 64-token block (scales [B, G, ceil(Tmax/64)])."""
+    B, G, Tmax, D = codes.shape
+    per_row = np.repeat(np.asarray(scales, dtype=np.float64), 64, axis=2)[:, :, :Tmax, None]
+    return e4m3_to_f64(codes) * per_row
+
+
+def gqa_decode_fp8_f64(q, k_codes, v_codes, k_scale, v_scale, seq_lens, scale, rows=None,
+                       threads: int = 1):
+    """The decode definition over the dequantised fp8 caches (KV-cache
+    quantisation changes only the element precision, "GQA analysis")."""
+    return get().gqa_decode_kv(q, dequantize_fp8(k_codes, k_scale), dequantize_fp8(v_codes, v_scale),
+                               seq_lens, scale, rows=rows, threads=threads)
 
 
 def get() -> Oracle:

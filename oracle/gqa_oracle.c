@@ -105,3 +105,66 @@ int oracle_gqa_decode_f64(const uint16_t* q, const uint16_t* k, const uint16_t* 
     free(x);
     return 0;
 }
+
+/*
+ * The same definition with K and V given as double values -- for caches whose
+ * elements are not bf16 (the fp8 cache, dequantised by the caller as code *
+ * block scale). q stays bf16 bits; k and v are [B, G, Tmax, D] double.
+ */
+int oracle_gqa_decode_kvf64(const uint16_t* q, const double* k, const double* v,
+                            const int32_t* seq_lens, double scale, int B, int sq, int H, int G,
+                            int D, int Tmax, long row_begin, long row_end, double* out,
+                            double* lse) {
+    if (B <= 0 || sq <= 0 || H <= 0 || G <= 0 || D <= 0 || Tmax <= 0) return -1;
+    if (H % G != 0) return -1;
+    long nrows = (long)B * sq * H;
+    if (row_begin < 0 || row_end > nrows || row_begin > row_end) return -1;
+    for (int b = 0; b < B; ++b)
+        if (seq_lens[b] < 0 || seq_lens[b] > Tmax) return -1;
+
+    const int heads_per_group = H / G;
+    double* x = (double*)malloc(sizeof(double) * (size_t)Tmax);
+    if (!x) return -1;
+
+    for (long r = row_begin; r < row_end; ++r) {
+        const int h = (int)(r % H);
+        const int s = (int)((r / H) % sq);
+        const int b = (int)(r / ((long)H * sq));
+        const int g = h / heads_per_group;
+        const int T = seq_lens[b];
+        const long last = (long)T - sq + s; /* last visible key index */
+
+        const uint16_t* qrow = q + (((long)b * sq + s) * H + h) * D;
+        const double* kbase = k + ((long)b * G + g) * (long)Tmax * D;
+        const double* vbase = v + ((long)b * G + g) * (long)Tmax * D;
+        double* orow = out + r * D;
+
+        if (last < 0) {
+            for (int d = 0; d < D; ++d) orow[d] = 0.0;
+            lse[r] = -INFINITY;
+            continue;
+        }
+        const long n = last + 1;
+
+        double mu = -INFINITY;
+        for (long t = 0; t < n; ++t) {
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += bf16_bits_to_double(qrow[d]) * kbase[t * D + d];
+            x[t] = scale * dot;
+            if (x[t] > mu) mu = x[t];
+        }
+
+        double Z = 0.0;
+        for (long t = 0; t < n; ++t) Z += exp(x[t] - mu);
+
+        for (int d = 0; d < D; ++d) orow[d] = 0.0;
+        for (long t = 0; t < n; ++t) {
+            double w = exp(x[t] - mu);
+            for (int d = 0; d < D; ++d) orow[d] += w * vbase[t * D + d];
+        }
+        for (int d = 0; d < D; ++d) orow[d] /= Z;
+        lse[r] = mu + log(Z);
+    }
+    free(x);
+    return 0;
+}

@@ -190,3 +190,30 @@ def paginate(k: np.ndarray, v: np.ndarray, seq_lens: np.ndarray, page_size: int,
             else:
                 table[b, j] = spare[(b + j) % len(spare)]
     return kp, vp, table
+
+
+E4M3_NAN = 0x7F
+
+
+def fp8_cache(bits: np.ndarray, seq_lens: np.ndarray, tail_code: int = E4M3_NAN):
+    """An fp8 (OCP E4M3) version of a bf16 cache [B, G, Tmax, D]: one fp32
+    scale per 64-token block of each (sequence, KV head), amax / 448 over the
+    block's valid rows (1 for a block with none), and codes = the e4m3
+    rounding (torch's float8_e4m3fn cast, round to nearest even) of
+    value / scale. Rows at or past a sequence's length get tail_code (NaN by
+    default). Returns (codes uint8 [B, G, Tmax, D], scales float32
+    [B, G, ceil(Tmax / 64)])."""
+    import torch
+    B, G, Tmax, D = bits.shape
+    nt = -(-Tmax // 64)
+    x = torch.from_numpy(bf16_bits_to_f32(bits).reshape(B, G, Tmax, D))
+    lens = np.clip(np.asarray(seq_lens, dtype=np.int64), 0, Tmax)
+    valid = torch.arange(Tmax)[None, :] < torch.from_numpy(lens)[:, None]          # [B, Tmax]
+    xv = torch.where(valid[:, None, :, None], x, torch.zeros(()))
+    pad = nt * 64 - Tmax
+    amax = torch.nn.functional.pad(xv.abs(), (0, 0, 0, pad)).reshape(B, G, nt, 64 * D).amax(-1)
+    scales = torch.where(amax > 0, amax / 448.0, torch.ones(()))                     # [B, G, nt]
+    per_row = scales.repeat_interleave(64, dim=2)[:, :, :Tmax, None]
+    codes = (x / per_row).to(torch.float8_e4m3fn).view(torch.uint8)
+    codes = torch.where(valid[:, None, :, None], codes, torch.full((), tail_code, dtype=torch.uint8))
+    return codes.numpy().copy(), scales.numpy().astype(np.float32).copy()
