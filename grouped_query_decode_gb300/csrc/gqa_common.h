@@ -91,8 +91,6 @@ struct KernelShape {
     static constexpr int kBoxes = D / kBoxElems;
     static constexpr int kTileBytes = kTileTokens * D * kElemBytes;   // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
-    // KV8: each consumer warp's fp16 copy of its 16 K and 16 V rows.
-    static constexpr int kStagingBytesPerWarp = KV8 ? 2 * 16 * D * 2 : 0;
     // Per row tile: the slice-merge buffer (3 slices x 16 x D floats), which
     // the cross-CTA merge reuses for a slot index, 16 maxima and 16 weights per
     // contributor.
@@ -102,12 +100,12 @@ struct KernelShape {
     static constexpr int kMergeBytes = MT * kMergeFloatsPerTile * 4;
     static constexpr int kMlBytes = MT * kSlices * 16 * 2 * 4;
     static constexpr int kQBytes = kConsumerWarps * kQBytesPerWarp;
-    static constexpr int kStagingBytes = kConsumerWarps * kStagingBytesPerWarp;
-    static constexpr int kStages = KV8 ? (MT == 1 ? 8 : 4) : (D == 128 ? (MT == 1 ? 5 : 4) : 8);
+    // fp8 stages are half as large: twice as many keep the same bytes in flight.
+    static constexpr int kStages = KV8 ? (MT == 1 ? 10 : 8) : (D == 128 ? (MT == 1 ? 5 : 4) : 8);
     static constexpr int kBarBytes = 8 * (2 * kStages + 4 * MT) + 64;
     // +1024 so the ring can be aligned to the 1 KB swizzle atom at run time.
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kMergeBytes + kMlBytes + kQBytes +
-                                      kStagingBytes + kBarBytes;
+    static constexpr int kSmemBytes =
+        1024 + kStages * kStageBytes + kMergeBytes + kMlBytes + kQBytes + kBarBytes;
 };
 
 }  // namespace gqa

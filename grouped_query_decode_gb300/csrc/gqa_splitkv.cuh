@@ -283,8 +283,7 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     float* merge_buf = reinterpret_cast<float*>(ring_ptr + S * KS::kStageBytes);
     float* ml_buf = merge_buf + KS::kMergeBytes / 4;
     unsigned char* q_smem = reinterpret_cast<unsigned char*>(ml_buf + KS::kMlBytes / 4);
-    unsigned char* staging = q_smem + KS::kQBytes;   // KV8 only; 512-byte aligned
-    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + KS::kStagingBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(q_smem + KS::kQBytes);
     const uint32_t full_bar = smem_addr(bars);
     const uint32_t empty_bar = full_bar + 8 * S;
     const uint32_t merge_bar = empty_bar + 8 * S;          // [MT][4]: A, B, C, D
@@ -455,6 +454,9 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     // P.V (B operand, transposed): matrix m -> d tile (m>>1), token half (m&1).
     const int v_tok = slice * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
     const int v_dt = lane >> 4;
+    // e4m3 K and V (one byte per element, one 128-byte box row per token):
+    // matrix m -> tokens 8*(m&1).., 16-byte chunk + (m>>1).
+    const int k8_tok = v_tok;
 
     uint32_t it = 0;
     uint32_t seg_parity = 0;   // phases of merge barriers A and B (every segment)
@@ -488,36 +490,65 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             if constexpr (!kQs) {
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; ++kk) {
-                    const int c = kk * 16 + 2 * quad;
-                    qa[kk][0] = q_lo ? __ldg(reinterpret_cast<const unsigned*>(q_lo + c)) : 0u;
-                    qa[kk][1] = q_hi ? __ldg(reinterpret_cast<const unsigned*>(q_hi + c)) : 0u;
-                    qa[kk][2] = q_lo ? __ldg(reinterpret_cast<const unsigned*>(q_lo + c + 8)) : 0u;
-                    qa[kk][3] = q_hi ? __ldg(reinterpret_cast<const unsigned*>(q_hi + c + 8)) : 0u;
-                    if constexpr (KV8) {   // fp16 MMAs: Q in fp16 (exact in fp16's range)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) qa[kk][e] = bf16x2_to_f16x2(qa[kk][e]);
+                    if constexpr (KV8) {
+                        // fp16 MMAs (Q converted exactly within fp16's range),
+                        // with the k order of the e4m3 K fragments: this thread's
+                        // k slots 2q, 2q+1 | 2q+8, 2q+9 hold d = 4q, 4q+1 | 4q+2,
+                        // 4q+3 of the step's 16 (the dot product is the same sum
+                        // in another order).
+                        const int c = kk * 16 + 4 * quad;
+                        const uint2 lo = q_lo ? __ldg(reinterpret_cast<const uint2*>(q_lo + c)) : make_uint2(0u, 0u);
+                        const uint2 hi = q_hi ? __ldg(reinterpret_cast<const uint2*>(q_hi + c)) : make_uint2(0u, 0u);
+                        qa[kk][0] = bf16x2_to_f16x2(lo.x);
+                        qa[kk][2] = bf16x2_to_f16x2(lo.y);
+                        qa[kk][1] = bf16x2_to_f16x2(hi.x);
+                        qa[kk][3] = bf16x2_to_f16x2(hi.y);
+                    } else {
+                        const int c = kk * 16 + 2 * quad;
+                        qa[kk][0] = q_lo ? __ldg(reinterpret_cast<const unsigned*>(q_lo + c)) : 0u;
+                        qa[kk][1] = q_hi ? __ldg(reinterpret_cast<const unsigned*>(q_hi + c)) : 0u;
+                        qa[kk][2] = q_lo ? __ldg(reinterpret_cast<const unsigned*>(q_lo + c + 8)) : 0u;
+                        qa[kk][3] = q_hi ? __ldg(reinterpret_cast<const unsigned*>(q_hi + c + 8)) : 0u;
                     }
                 }
             } else {
                 // This warp's 16 Q rows into its own shared-memory copy, 16-byte
                 // chunks swizzled by row so that ldmatrix reads are conflict free.
-                for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
-                    const int row = idx / (D / 8), chunk = idx % (D / 8);
-                    const int r = mt * 16 + row;
-                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (r < p.R) {
-                        const int j = r / p.sq, sq_i = r % p.sq;
-                        const int qrow = (sg.b * p.sq + sq_i) * p.H + sg.g * p.heads_per_group + j;
-                        v = __ldg(reinterpret_cast<const uint4*>(p.q + (size_t)qrow * D) + chunk);
-                        if constexpr (KV8) {
-                            v.x = bf16x2_to_f16x2(v.x);
-                            v.y = bf16x2_to_f16x2(v.y);
-                            v.z = bf16x2_to_f16x2(v.z);
-                            v.w = bf16x2_to_f16x2(v.w);
+                unsigned char* qw = q_smem + warp * KS::kQBytesPerWarp;
+                if constexpr (KV8) {
+                    // fp16, each 16-wide k step stored as the A fragments of the
+                    // e4m3 k order: chunk 2c holds d {0,1,4,5,8,9,12,13} of step
+                    // c, chunk 2c+1 d {2,3,6,7,10,11,14,15}.
+                    for (int idx = lane; idx < 16 * (D / 16); idx += 32) {
+                        const int row = idx / (D / 16), c16 = idx % (D / 16);
+                        const int r = mt * 16 + row;
+                        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+                        if (r < p.R) {
+                            const int j = r / p.sq, sq_i = r % p.sq;
+                            const int qrow = (sg.b * p.sq + sq_i) * p.H + sg.g * p.heads_per_group + j;
+                            const uint4* src = reinterpret_cast<const uint4*>(p.q + (size_t)qrow * D) + 2 * c16;
+                            a = __ldg(src);
+                            b = __ldg(src + 1);
                         }
+                        const uint4 ev = make_uint4(bf16x2_to_f16x2(a.x), bf16x2_to_f16x2(a.z),
+                                                    bf16x2_to_f16x2(b.x), bf16x2_to_f16x2(b.z));
+                        const uint4 od = make_uint4(bf16x2_to_f16x2(a.y), bf16x2_to_f16x2(a.w),
+                                                    bf16x2_to_f16x2(b.y), bf16x2_to_f16x2(b.w));
+                        *reinterpret_cast<uint4*>(qw + row * (D * 2) + (((2 * c16) ^ (row & 7)) << 4)) = ev;
+                        *reinterpret_cast<uint4*>(qw + row * (D * 2) + (((2 * c16 + 1) ^ (row & 7)) << 4)) = od;
                     }
-                    *reinterpret_cast<uint4*>(q_smem + warp * KS::kQBytesPerWarp + row * (D * 2) +
-                                              ((chunk ^ (row & 7)) << 4)) = v;
+                } else {
+                    for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
+                        const int row = idx / (D / 8), chunk = idx % (D / 8);
+                        const int r = mt * 16 + row;
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        if (r < p.R) {
+                            const int j = r / p.sq, sq_i = r % p.sq;
+                            const int qrow = (sg.b * p.sq + sq_i) * p.H + sg.g * p.heads_per_group + j;
+                            v = __ldg(reinterpret_cast<const uint4*>(p.q + (size_t)qrow * D) + chunk);
+                        }
+                        *reinterpret_cast<uint4*>(qw + row * (D * 2) + ((chunk ^ (row & 7)) << 4)) = v;
+                    }
                 }
                 __syncwarp();
             }
@@ -559,54 +590,14 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             const uint32_t vst = kst + KS::kTileBytes;
             const int tbase = (sg.t0 + i) * kTileTokens;
 
-            // KV8: this warp's 16 K and V rows, e4m3 codes, into its fp16
-            // staging copy (the same swizzled layout as a bf16 stage, 16 rows
-            // high); V rows past the valid length become 0. The fp8 stage is
-            // then released at once. Every e4m3 value is an fp16 value, so the
-            // copy is exact; the scales are applied to the scores and to P.
-            uint32_t k_src = kst, v_src = vst;
-            int k_row0 = slice * 16, box_stride = kTileTokens * 128;
-            if constexpr (KV8) {
-                const uint32_t stk = smem_addr(staging) + warp * KS::kStagingBytesPerWarp;
-                const uint32_t stv = stk + 16 * D * 2;
-                __syncwarp();   // this warp's previous reads of its staging are done
-                for (int u = lane; u < 2 * 16 * (D / 16); u += 32) {
-                    const int is_v = u >= 16 * (D / 16);
-                    const int uu = is_v ? u - 16 * (D / 16) : u;
-                    const int row = uu / (D / 16), c8 = uu % (D / 16);   // 16 codes per chunk
-                    const int srow = slice * 16 + row;
-                    const uint4 codes = ld_shared_v4((is_v ? vst : kst) + (c8 >> 3) * (kTileTokens * 128) +
-                                                     srow * 128 + (((c8 & 7) ^ (srow & 7)) << 4));
-                    uint4 h0, h1;
-                    if (is_v && tbase + srow >= sg.tb) {
-                        h0 = make_uint4(0u, 0u, 0u, 0u);
-                        h1 = h0;
-                    } else {
-                        h0 = make_uint4(e4m3x2_to_f16x2((uint16_t)codes.x), e4m3x2_to_f16x2((uint16_t)(codes.x >> 16)),
-                                        e4m3x2_to_f16x2((uint16_t)codes.y), e4m3x2_to_f16x2((uint16_t)(codes.y >> 16)));
-                        h1 = make_uint4(e4m3x2_to_f16x2((uint16_t)codes.z), e4m3x2_to_f16x2((uint16_t)(codes.z >> 16)),
-                                        e4m3x2_to_f16x2((uint16_t)codes.w), e4m3x2_to_f16x2((uint16_t)(codes.w >> 16)));
-                    }
-                    const int c16 = 2 * c8;                       // first fp16 chunk
-                    const uint32_t dst = (is_v ? stv : stk) + (c16 >> 3) * (16 * 128) + row * 128;
-                    st_shared_v4(dst + (((c16 & 7) ^ (row & 7)) << 4), h0);
-                    st_shared_v4(dst + ((((c16 + 1) & 7) ^ (row & 7)) << 4), h1);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar + 8 * s);
-                k_src = stk;
-                v_src = stv;
-                k_row0 = 0;
-                box_stride = 16 * 128;
-            }
-
             // Rows past the valid length may hold anything (NaN included);
             // zero them in V so that p = 0 times them stays 0.
-            if (!KV8 && tbase + kTileTokens > sg.tb) {
+            if (tbase + kTileTokens > sg.tb) {
+                constexpr int kChunks = D * KS::kElemBytes / 16;   // 16-byte chunks per row
                 bool wrote = false;
-                for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
-                    const int row = slice * 16 + idx / (D / 8);
-                    const int chunk = idx % (D / 8);
+                for (int idx = lane; idx < 16 * kChunks; idx += 32) {
+                    const int row = slice * 16 + idx / kChunks;
+                    const int chunk = idx % kChunks;
                     if (tbase + row >= sg.tb) {
                         const int bx = chunk >> 3, cc = chunk & 7;
                         st_shared_zero16(vst + bx * (kTileTokens * 128) + row * 128 +
@@ -653,23 +644,43 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
 
             // S = Q K^T for this warp's 16 tokens: two n8 tiles.
             float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            const int kt = k_tok - slice * 16 + k_row0;   // K row in the tile being read
+            if constexpr (KV8) {
+                // e4m3 codes straight from the stage: an 8x8 b16 ldmatrix of K
+                // rows gives each thread 4 consecutive codes (d = 4q..4q+3 of a
+                // 16-wide k step) of one token, i.e. both B registers of that
+                // step in the k order the Q fragments were given. One x4 load
+                // covers 2 tokens tiles x 2 k steps.
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-                const int chunk = kk * 2 + k_half;
-                const int bx = chunk >> 3, cc = chunk & 7;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(k_src + bx * box_stride + kt * 128 + ((cc ^ (kt & 7)) << 4), b0, b1, b2, b3);
-                uint32_t a_s[4];
-                if constexpr (kQs) {
-                    const int qc = kk * 2 + (lane >> 4);
-                    ldsm_x4(qa_base + ((qc ^ (qa_row & 7)) << 4), a_s[0], a_s[1], a_s[2], a_s[3]);
+                for (int kk = 0; kk < KSTEPS; kk += 2) {
+                    const int c8 = kk + (lane >> 4);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4(kst + k8_tok * 128 + ((c8 ^ (k8_tok & 7)) << 4), r0, r1, r2, r3);
+                    uint32_t a0_s[4], a1_s[4];
+                    if constexpr (kQs) {
+                        const int qc = kk * 2 + (lane >> 4);
+                        ldsm_x4(qa_base + ((qc ^ (qa_row & 7)) << 4), a0_s[0], a0_s[1], a0_s[2], a0_s[3]);
+                        ldsm_x4(qa_base + (((qc + 2) ^ (qa_row & 7)) << 4), a1_s[0], a1_s[1], a1_s[2], a1_s[3]);
+                    }
+                    const uint32_t(&a0)[4] = kQs ? a0_s : qa[kQs ? 0 : kk];
+                    const uint32_t(&a1)[4] = kQs ? a1_s : qa[kQs ? 0 : kk + 1];
+                    mma_f16_16816(sc[0], a0, e4m3x2_to_f16x2((uint16_t)r0), e4m3x2_to_f16x2((uint16_t)(r0 >> 16)));
+                    mma_f16_16816(sc[1], a0, e4m3x2_to_f16x2((uint16_t)r1), e4m3x2_to_f16x2((uint16_t)(r1 >> 16)));
+                    mma_f16_16816(sc[0], a1, e4m3x2_to_f16x2((uint16_t)r2), e4m3x2_to_f16x2((uint16_t)(r2 >> 16)));
+                    mma_f16_16816(sc[1], a1, e4m3x2_to_f16x2((uint16_t)r3), e4m3x2_to_f16x2((uint16_t)(r3 >> 16)));
                 }
-                const uint32_t(&a)[4] = kQs ? a_s : qa[kQs ? 0 : kk];
-                if constexpr (KV8) {
-                    mma_f16_16816(sc[0], a, b0, b1);
-                    mma_f16_16816(sc[1], a, b2, b3);
-                } else {
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const int chunk = kk * 2 + k_half;
+                    const int bx = chunk >> 3, cc = chunk & 7;
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kst + bx * (kTileTokens * 128) + k_tok * 128 + ((cc ^ (k_tok & 7)) << 4), b0, b1, b2, b3);
+                    uint32_t a_s[4];
+                    if constexpr (kQs) {
+                        const int qc = kk * 2 + (lane >> 4);
+                        ldsm_x4(qa_base + ((qc ^ (qa_row & 7)) << 4), a_s[0], a_s[1], a_s[2], a_s[3]);
+                    }
+                    const uint32_t(&a)[4] = kQs ? a_s : qa[kQs ? 0 : kk];
                     mma_bf16_16816(sc[0], a, b0, b1);
                     mma_bf16_16816(sc[1], a, b2, b3);
                 }
@@ -750,25 +761,43 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                 pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
                 pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
             }
-            const int vt = v_tok - slice * 16 + k_row0;   // V row in the tile being read
+            if constexpr (KV8) {
+                // e4m3 V: a transposed 8x8 b16 ldmatrix of V rows gives each
+                // thread codes d = 2n, 2n+1 (n = lane / 4) of tokens 2q and
+                // 2q+1. A byte permute splits them into the B registers of two
+                // "virtual" n8 tiles: o[2c] holds the even columns 16c + 2n of
+                // 16-wide chunk c, o[2c+1] the odd ones; the writes below put
+                // the columns back in order.
 #pragma unroll
-            for (int n = 0; n < NTILE_D; n += 2) {
-                const int chunk = n + v_dt;
-                const int bx = chunk >> 3, cc = chunk & 7;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(v_src + bx * box_stride + vt * 128 + ((cc ^ (vt & 7)) << 4), b0, b1, b2, b3);
-                if constexpr (KV8) {
-                    mma_f16_16816(o[n], pa, b0, b1);
-                    mma_f16_16816(o[n + 1], pa, b2, b3);
-                } else {
+                for (int blk = 0; blk < D / 16; blk += 2) {
+                    const int c8 = blk + (lane >> 4);
+                    uint32_t r[4];
+                    ldsm_x4_trans(vst + k8_tok * 128 + ((c8 ^ (k8_tok & 7)) << 4), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const uint32_t lo = r[2 * e], hi = r[2 * e + 1];   // tokens 0-7, 8-15
+                        mma_f16_16816(o[2 * (blk + e)], pa,
+                                      e4m3x2_to_f16x2((uint16_t)__byte_perm(lo, 0u, 0x0020)),
+                                      e4m3x2_to_f16x2((uint16_t)__byte_perm(hi, 0u, 0x0020)));
+                        mma_f16_16816(o[2 * (blk + e) + 1], pa,
+                                      e4m3x2_to_f16x2((uint16_t)__byte_perm(lo, 0u, 0x0031)),
+                                      e4m3x2_to_f16x2((uint16_t)__byte_perm(hi, 0u, 0x0031)));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int n = 0; n < NTILE_D; n += 2) {
+                    const int chunk = n + v_dt;
+                    const int bx = chunk >> 3, cc = chunk & 7;
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_trans(vst + bx * (kTileTokens * 128) + v_tok * 128 + ((cc ^ (v_tok & 7)) << 4), b0, b1,
+                                  b2, b3);
                     mma_bf16_16816(o[n], pa, b0, b1);
                     mma_bf16_16816(o[n + 1], pa, b2, b3);
                 }
             }
-            if constexpr (!KV8) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar + 8 * s);
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar + 8 * s);
         }
         if (failed) break;
 
@@ -838,19 +867,35 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             if (slice != 0) continue;
             if (out_lo >= 0) {
                 uint16_t* orow = p.out + (size_t)out_lo * D;
+                if constexpr (KV8) {
 #pragma unroll
-                for (int n = 0; n < NTILE_D; ++n)
-                    *reinterpret_cast<uint32_t*>(orow + n * 8 + 2 * quad) =
-                        pack_bf16x2(o[n][0] * inv_lo, o[n][1] * inv_lo);
+                    for (int c = 0; c < D / 16; ++c)
+                        *reinterpret_cast<uint2*>(orow + 16 * c + 4 * quad) =
+                            make_uint2(pack_bf16x2(o[2 * c][0] * inv_lo, o[2 * c + 1][0] * inv_lo),
+                                       pack_bf16x2(o[2 * c][1] * inv_lo, o[2 * c + 1][1] * inv_lo));
+                } else {
+#pragma unroll
+                    for (int n = 0; n < NTILE_D; ++n)
+                        *reinterpret_cast<uint32_t*>(orow + n * 8 + 2 * quad) =
+                            pack_bf16x2(o[n][0] * inv_lo, o[n][1] * inv_lo);
+                }
                 if (p.lse && quad == 0)
                     p.lse[out_lo] = L_lo > 0.f ? (M_lo + log2f(L_lo)) * 0.69314718055994531f : -INFINITY;
             }
             if (out_hi >= 0) {
                 uint16_t* orow = p.out + (size_t)out_hi * D;
+                if constexpr (KV8) {
 #pragma unroll
-                for (int n = 0; n < NTILE_D; ++n)
-                    *reinterpret_cast<uint32_t*>(orow + n * 8 + 2 * quad) =
-                        pack_bf16x2(o[n][2] * inv_hi, o[n][3] * inv_hi);
+                    for (int c = 0; c < D / 16; ++c)
+                        *reinterpret_cast<uint2*>(orow + 16 * c + 4 * quad) =
+                            make_uint2(pack_bf16x2(o[2 * c][2] * inv_hi, o[2 * c + 1][2] * inv_hi),
+                                       pack_bf16x2(o[2 * c][3] * inv_hi, o[2 * c + 1][3] * inv_hi));
+                } else {
+#pragma unroll
+                    for (int n = 0; n < NTILE_D; ++n)
+                        *reinterpret_cast<uint32_t*>(orow + n * 8 + 2 * quad) =
+                            pack_bf16x2(o[n][2] * inv_hi, o[n][3] * inv_hi);
+                }
                 if (p.lse && quad == 0)
                     p.lse[out_hi] = L_hi > 0.f ? (M_hi + log2f(L_hi)) * 0.69314718055994531f : -INFINITY;
             }
@@ -867,20 +912,36 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             float* om = slot + (size_t)p.R * D;
             float* ol = om + p.R;
             if (r_lo < p.R) {
+                if constexpr (KV8) {
 #pragma unroll
-                for (int n = 0; n < NTILE_D; ++n)
-                    __stcg(reinterpret_cast<float2*>(slot + (size_t)r_lo * D + n * 8 + 2 * quad),
-                           make_float2(o[n][0] * inv_lo, o[n][1] * inv_lo));
+                    for (int c = 0; c < D / 16; ++c)
+                        __stcg(reinterpret_cast<float4*>(slot + (size_t)r_lo * D + 16 * c + 4 * quad),
+                               make_float4(o[2 * c][0] * inv_lo, o[2 * c + 1][0] * inv_lo,
+                                           o[2 * c][1] * inv_lo, o[2 * c + 1][1] * inv_lo));
+                } else {
+#pragma unroll
+                    for (int n = 0; n < NTILE_D; ++n)
+                        __stcg(reinterpret_cast<float2*>(slot + (size_t)r_lo * D + n * 8 + 2 * quad),
+                               make_float2(o[n][0] * inv_lo, o[n][1] * inv_lo));
+                }
                 if (quad == 0) {
                     __stcg(om + r_lo, M_lo);
                     __stcg(ol + r_lo, L_lo);
                 }
             }
             if (r_hi < p.R) {
+                if constexpr (KV8) {
 #pragma unroll
-                for (int n = 0; n < NTILE_D; ++n)
-                    __stcg(reinterpret_cast<float2*>(slot + (size_t)r_hi * D + n * 8 + 2 * quad),
-                           make_float2(o[n][2] * inv_hi, o[n][3] * inv_hi));
+                    for (int c = 0; c < D / 16; ++c)
+                        __stcg(reinterpret_cast<float4*>(slot + (size_t)r_hi * D + 16 * c + 4 * quad),
+                               make_float4(o[2 * c][2] * inv_hi, o[2 * c + 1][2] * inv_hi,
+                                           o[2 * c][3] * inv_hi, o[2 * c + 1][3] * inv_hi));
+                } else {
+#pragma unroll
+                    for (int n = 0; n < NTILE_D; ++n)
+                        __stcg(reinterpret_cast<float2*>(slot + (size_t)r_hi * D + n * 8 + 2 * quad),
+                               make_float2(o[n][2] * inv_hi, o[n][3] * inv_hi));
+                }
                 if (quad == 0) {
                     __stcg(om + r_hi, M_hi);
                     __stcg(ol + r_hi, L_hi);
