@@ -69,6 +69,22 @@ def algorithmic_flops(sq: int, H: int, D: int, lens) -> int:
     return 4 * sq * H * D * int(np.sum(np.asarray(lens, dtype=np.int64)))
 
 
+def visible_keys(sq: int, lens) -> int:
+    """Keys all query rows of one head see: new token s of sequence b attends
+    to positions t <= T_b - sq + s, i.e. max(0, T_b - sq + s + 1) keys."""
+    total = 0
+    for t in np.asarray(lens, dtype=np.int64):
+        s = np.arange(sq, dtype=np.int64)
+        total += int(np.maximum(0, t - sq + s + 1).sum())
+    return total
+
+
+def prefill_flops(H: int, D: int, sq: int, lens) -> int:
+    """QK^T and PV over the visible (causal) keys only: 2 x 2 flops per key per
+    head dimension element per query row."""
+    return 4 * H * D * visible_keys(sq, lens)
+
+
 # --------------------------------------------------------------- helpers
 
 def _peaks():
@@ -211,6 +227,26 @@ def run_reference(args, cfg):
     if rank != 0:
         return 0
     q, k, v, lens = syn.make_inputs(cfg, tail_bits=syn.BF16_ZERO)
+    if cfg in syn.PREFILL_CONFIGS:
+        # A whole prefill takes the oracle minutes: each step is the bounded
+        # sample of the CPU baseline (the last new tokens, every head).
+        rates = []
+        for _ in range(max(1, args.steps)):
+            rate, threads, sample = time_oracle_prefill(cfg, q, k, v, lens, 0)
+            rates.append(rate)
+        value = statistics.median(rates)
+        line = {
+            "impl": "reference", "metric": "prefill attention TFLOP/s (causal keys only) at 1 GPU",
+            "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config_dict(cfg, lens, l2_note="host memory"),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
+        return 0
     nbytes = algorithmic_bytes(cfg.B, cfg.sq, cfg.H, cfg.G, cfg.D, lens)
     time_oracle(cfg, q, k, v, lens, 0, max_reps=max(1, args.warmup))
     times, threads = time_oracle(cfg, q, k, v, lens, 0, max_reps=args.steps)
@@ -481,13 +517,189 @@ def run_gpu(args, cfg):
     return 0
 
 
+# ------------------------------------------------------- prefill GPU arm
+
+def _tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def time_oracle_prefill(cfg, q, k, v, lens, budget_s: float, rows_tokens: int = 16):
+    """The oracle (as it stands) on a bounded sample of a prefill: the last
+    `rows_tokens` new tokens of every sequence (all heads), which see the most
+    keys. Returns (TFLOP/s, threads, description)."""
+    import oracle
+    threads = os.cpu_count() or 1
+    orc = oracle.get()
+    n = min(rows_tokens, cfg.sq)
+    qs = np.ascontiguousarray(q[:, cfg.sq - n:])
+    flops = 4 * cfg.H * cfg.D * visible_keys(n, lens)
+    times = []
+    t_all = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        orc.gqa_decode(qs, k, v, lens, cfg.scale, threads=threads)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_all >= budget_s:
+            break
+    tc = statistics.median(times)
+    return flops / tc / 1e12, threads, (f"last {n} new tokens of each of the {cfg.B} sequences "
+                                        f"({cfg.B * n * cfg.H} query rows), {len(times)} repetitions, median")
+
+
+def run_gpu_prefill(args, cfg):
+    import torch
+    import torch.distributed as dist
+
+    import grouped_query_decode_gb300 as gq
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    q, k, v, lens = syn.make_inputs(cfg, tail_bits=syn.BF16_ZERO)
+    flops = prefill_flops(cfg.H, cfg.D, cfg.sq, lens)
+    nbytes = algorithmic_bytes(cfg.B, cfg.sq, cfg.H, cfg.G, cfg.D, lens)
+
+    def to_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    cache_bytes = 2 * k.nbytes
+    copies = max(2, math.ceil(4 * l2 / cache_bytes))
+    dq = to_dev(q)
+    dl = torch.from_numpy(lens).to(dev)
+    dks = [to_dev(k) for _ in range(copies)]
+    dvs = [to_dev(v) for _ in range(copies)]
+    out = torch.empty(cfg.B, cfg.sq, cfg.H, cfg.D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(cfg.B, cfg.sq, cfg.H, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        c = i % copies
+        gq.gqa_prefill(dq, dks[c], dvs[c], dl, cfg.scale, out, lse, stream=stream)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    assert gq.gqa_decode_check_error(stream) == gq.GQA_OK
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.15)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    ms_total = e0.elapsed_time(e1)
+    t_tail = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t_tail < max(0.0, 0.6 - t_wall):
+        step(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    sampler.stop()
+    clocks = sampler.summary()
+    clocks["window"] = "timed region" if t_wall >= 0.6 else "timed region + untimed tail of the same step"
+    assert gq.gqa_decode_check_error(stream) == gq.GQA_OK
+
+    ms_step, _ = aggregate_over_ranks(ms_total / args.steps, nbytes, device=dev)
+    value = ws * flops / (ms_step * 1e-3) / 1e12
+    kernel_ms = ms_total / args.steps
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    peak, peak_kind = _tensor_peak()
+
+    # End to end: inputs from pinned host memory, outputs back, every step.
+    hq = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hk = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hv = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hl = torch.from_numpy(lens).pin_memory()
+    ho = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dks[0].copy_(hk, non_blocking=True)
+        dvs[0].copy_(hv, non_blocking=True)
+        dl.copy_(hl, non_blocking=True)
+        gq.gqa_prefill(dq, dks[0], dvs[0], dl, cfg.scale, out, lse, stream=stream)
+        ho.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    e2e_steps = max(3, min(args.steps, 20))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms, _ = aggregate_over_ranks(a.elapsed_time(b) / e2e_steps, nbytes, device=dev)
+
+    if rank == 0:
+        cpu = None
+        if ws == 1 and not args.no_cpu_baseline:
+            rate, threads, sample = time_oracle_prefill(cfg, q, k, v, lens, args.cpu_budget_s)
+            cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample}
+        line = {
+            "metric": "prefill attention TFLOP/s (causal keys only) at 1 GPU", "value": value,
+            "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_step, "us_per_step": ms_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": _config_dict(cfg, lens, l2_note=f"{copies} rotating K/V copies of "
+                                                      f"{cache_bytes >> 20} MiB vs {l2 >> 20} MiB L2"),
+            "query_tokens_per_s": ws * cfg.B * cfg.sq / (ms_step * 1e-3),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                         "kernel": "gqa_prefill_kernel", "duration_us": kernel_ms * 1e3,
+                         "duration": f"average over the {args.steps} launches of the timed region "
+                                     "(CUDA events on the launching stream; one launch per step)",
+                         "algorithmic_flops_per_launch": flops},
+            "cpu_baseline": cpu,
+            "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "us_per_step": e2e_ms * 1e3,
+                    "h2d_bytes_per_step": hq.nbytes + hk.nbytes + hv.nbytes + hl.nbytes,
+                    "d2h_bytes_per_step": ho.nbytes + hlse.nbytes},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=[c.name for c in syn.CONFIGS])
+                    choices=[c.name for c in syn.CONFIGS + syn.PREFILL_CONFIGS],
+                    help="a decode workload, or a prefill workload (timed on gqa_prefill)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -501,6 +713,8 @@ def main(argv=None):
     cfg = syn.config_by_name(args.workload)
     if args.impl == "reference":
         return run_reference(args, cfg)
+    if cfg in syn.PREFILL_CONFIGS:
+        return run_gpu_prefill(args, cfg)
     return run_gpu(args, cfg)
 
 

@@ -68,6 +68,8 @@ def load():
             lib.gqa_decode_paged.restype = i32
             lib.gqa_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, vp, *shape, vp]
             lib.gqa_decode_fp8.restype = i32
+            lib.gqa_prefill.argtypes = [vp, vp, vp, vp, f32, vp, vp, *shape, vp]
+            lib.gqa_prefill.restype = i32
             lib.gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, f32, vp, vp, *shape, vp]
             lib.gqa_decode_noalloc.restype = i32
             lib.gqa_decode_workspace_bytes.argtypes = shape
@@ -138,6 +140,19 @@ def gqa_decode(q, k_cache, v_cache, seq_lens, scale, out, lse=None, stream=None)
                            _stream_handle(stream, q.device))
     if rc != GQA_OK:
         raise GQADecodeError(rc, "gqa_decode")
+
+
+def gqa_prefill(q, k_cache, v_cache, seq_lens, scale, out, lse=None, stream=None):
+    """Prefill or chunked prefill: the same attention as gqa_decode for any
+    number of new tokens sq (no limit on (H/G)*sq), on the tcgen05 kernel.
+    The sq new tokens' K/V must already be in the cache; seq_lens counts them."""
+    B, sq, H, G, D, Tmax = _shapes(q, k_cache, v_cache, seq_lens, out, lse)
+    rc = load().gqa_prefill(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                            seq_lens.data_ptr(), float(scale), out.data_ptr(),
+                            None if lse is None else lse.data_ptr(), B, sq, H, G, D, Tmax,
+                            _stream_handle(stream, q.device))
+    if rc != GQA_OK:
+        raise GQADecodeError(rc, "gqa_prefill")
 
 
 def gqa_decode_append(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out, lse=None,

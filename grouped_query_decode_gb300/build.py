@@ -15,7 +15,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libgqa_decode.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
-SOURCES = ["api.cu", "api_noalloc.cu", "splitkv_d64.cu", "splitkv_d128.cu", "splitkv_d128_fp8.cu"]
+SOURCES = ["api.cu", "api_noalloc.cu", "splitkv_d64.cu", "splitkv_d128.cu", "splitkv_d128_fp8.cu",
+           "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -398,6 +398,51 @@ int gqa_decode_fp8(const void* q, const void* k_codes, const void* v_codes, cons
                    stream, nullptr, nullptr, Paging(), f8);
 }
 
+int gqa_prefill(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
+                float scale, void* out, float* lse, int B, int sq, int H, int G, int D, int Tmax,
+                cudaStream_t stream) {
+    if (B <= 0 || sq <= 0 || H <= 0 || G <= 0 || D <= 0 || Tmax <= 0) return GQA_ERR_INVALID_ARG;
+    if (H % G != 0) return GQA_ERR_HEAD_RATIO;
+    if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
+    if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(seq_lens) ||
+        !aligned16(out) || (lse && !aligned16(lse)))
+        return GQA_ERR_MISALIGNED;
+    const long long R = (long long)(H / G) * sq;
+    const long long row_tiles = (R + 127) / 128;
+    if ((long long)B * sq * H >= (1ll << 31) || R >= (1ll << 31) ||
+        (long long)B * G * row_tiles >= (1ll << 31))
+        return GQA_ERR_UNSUPPORTED;
+    DeviceInfo info;
+    int st = device_info(&info);
+    if (st != GQA_OK) return st;
+    PrefillLaunchArgs a{};
+    st = encode_cache_map(&a.tm_k, k_cache, (long long)B * G, Tmax, D, 128);
+    if (st != GQA_OK) return st;
+    st = encode_cache_map(&a.tm_v, v_cache, (long long)B * G, Tmax, D, 128);
+    if (st != GQA_OK) return st;
+    a.p.q = static_cast<const uint16_t*>(q);
+    a.p.seq_lens = seq_lens;
+    a.p.out = static_cast<uint16_t*>(out);
+    a.p.lse = lse;
+    a.p.status = info.status;
+    a.p.scale_log2 = scale * 1.4426950408889634f;
+    a.p.B = B;
+    a.p.sq = sq;
+    a.p.H = H;
+    a.p.G = G;
+    a.p.Tmax = Tmax;
+    a.p.R = (int)R;
+    a.p.heads_per_group = H / G;
+    a.p.row_tiles = (int)row_tiles;
+    debug_knobs(&a.p.wait_timeout_ns, &a.p.skip_tile);
+    a.grid = (unsigned)((long long)B * G * row_tiles);
+    a.stream = stream;
+    cudaError_t e = launch_prefill(D, a);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return GQA_OK;
+}
+
 int gqa_decode_check_error(cudaStream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e);

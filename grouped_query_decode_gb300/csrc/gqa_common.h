@@ -69,6 +69,19 @@ struct DecodeParams {
     int scale_tiles;
 };
 
+// Prefill kernel parameters (one CTA per 128-row tile of one (b, g) unit).
+struct PrefillParams {
+    const uint16_t* q;        // [B, sq, H, D] bf16
+    const int32_t* seq_lens;  // [B]
+    uint16_t* out;            // [B, sq, H, D] bf16
+    float* lse;               // [B, sq, H] or nullptr
+    unsigned* status;         // per-device status word
+    unsigned long long wait_timeout_ns;
+    float scale_log2;
+    int B, sq, H, G, Tmax, R, heads_per_group, row_tiles;
+    int skip_tile;            // fault injection for tests (-1: off)
+};
+
 // One CTA per SM. Every 16-row tile of the group has four consumer warps
 // ("slices") that take 16 of a stage's 64 tokens each; one more warp issues
 // the TMA copies. With two row tiles (9 warps, which the register file

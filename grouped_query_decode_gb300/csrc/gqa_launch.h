@@ -24,6 +24,17 @@ cudaError_t launch_d64(const LaunchArgs& a);
 cudaError_t launch_d128(const LaunchArgs& a);
 cudaError_t launch_d128_fp8(const LaunchArgs& a);
 
+// The prefill kernel: one CTA per 128-row tile of one (sequence, KV head).
+struct PrefillLaunchArgs {
+    CUtensorMap tm_k;
+    CUtensorMap tm_v;
+    PrefillParams p;
+    unsigned grid;
+    cudaStream_t stream;
+};
+cudaError_t launch_prefill(int D, const PrefillLaunchArgs& a);
+int prefill_smem_bytes(int D);
+
 // Dynamic shared memory and threads per CTA of the split-KV kernel.
 int splitkv_smem_bytes(int D, int row_tiles, bool kv8 = false);
 int splitkv_threads(int D, int row_tiles, bool kv8 = false);

@@ -26,6 +26,7 @@
 #include <cstdint>
 
 #include "gqa_common.h"
+#include "gqa_device.cuh"
 #include "ptx.cuh"
 
 namespace gqa {
@@ -38,8 +39,6 @@ struct Segment {
     bool complete;       // the segment covers the whole unit
     bool first;          // the CTA's first segment (partial slot 0, else slot 1)
 };
-
-__device__ __forceinline__ int clamp_len(int t, int Tmax) { return t < 0 ? 0 : (t > Tmax ? Tmax : t); }
 
 __device__ __forceinline__ long long tiles_of(int tb) { return (tb + kTileTokens - 1) / kTileTokens; }
 
@@ -80,23 +79,6 @@ struct SegmentWalker {
         return false;
     }
 };
-
-// Bounded wait on an mbarrier phase. On expiry, or when another warp of the
-// CTA has already given up, it records the failure and returns false.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                           unsigned* status, uint64_t timeout_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > timeout_ns) {
-            *abort_flag = 1;
-            atomicOr(status, kStatusTimeout);
-            return false;
-        }
-    }
-}
 
 // Counts one arrival on a unit's counter and returns the arrivals so far in
 // this call. The counter holds (epoch << 16) | count; the first arrival of a

@@ -148,6 +148,28 @@ int gqa_decode_fp8(const void* q, const void* k_codes, const void* v_codes, cons
                    int B, int sq, int H, int G, int D, int Tmax, cudaStream_t stream);
 
 /*
+ * Prefill and chunked prefill: the attention of gqa_decode for any number of
+ * new tokens per sequence. Section 7 of "Same GQA, Different Execution Cost
+ * Across Backends" ("in prefill, merge the group into the sequence axis")
+ * folds the H/G query heads that share a KV head into the row axis,
+ * [B, Hkv, G x M, D], so each KV head's K and V serve all (H/G) * sq of its
+ * rows at once, and each row keeps its own causal limit and softmax. Same
+ * arguments, layouts, causal rule (new token s at position T_b - sq + s sees
+ * keys t <= T_b - sq + s), outputs and error codes as gqa_decode, with no
+ * bound on (H/G) * sq; D in {64, 128}. A fresh prefill has T_b = sq; a
+ * chunked prefill has the earlier chunks' K/V in the cache as well.
+ *
+ * The products run on the tcgen05 tensor cores (bf16 inputs, fp32
+ * accumulation in tensor memory, probabilities rounded to bf16 for P.V). No
+ * workspace: one CTA computes each 128-row tile of one (sequence, KV head)
+ * over its whole key range. Asynchronous on `stream`; a bounded device-side
+ * wait that expires is reported by gqa_decode_check_error().
+ */
+int gqa_prefill(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
+                float scale, void* out, float* lse, int B, int sq, int H, int G, int D, int Tmax,
+                cudaStream_t stream);
+
+/*
  * Bytes of device workspace gqa_decode_ex needs for these sizes on the current
  * device: two partial-result slots (O[R][D], running max m[R], sum l[R]) per
  * split-KV CTA plus the per-sequence tile prefix sums. Returns 0 for

@@ -17,7 +17,7 @@ from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
-from .configs import CONFIGS, DecodeConfig, config_by_name  # noqa: F401
+from .configs import CONFIGS, PREFILL_CONFIGS, DecodeConfig, config_by_name  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gen.c")

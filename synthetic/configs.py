@@ -66,8 +66,27 @@ CONFIGS = [
 ]
 
 
+# Prefill and chunked-prefill workloads (many new tokens per sequence, causal
+# among themselves). The first is the chunk of section 7 of "Same GQA,
+# Different Execution Cost Across Backends": q_len = 64 new tokens, 32 query
+# heads over 8 KV heads, head_dim 64, at the end of a 4096-token context.
+PREFILL_CONFIGS = [
+    DecodeConfig("chunked_prefill_q64_d64", B=1, sq=64, H=32, G=8, D=64, Tmax=4096, t_lo=4096,
+                 t_hi=4096, seed=_BASE_SEED + 21,
+                 note="64-token chunk after 4032 cached tokens, 32 heads over 8, D = 64"),
+    DecodeConfig("prefill_d64_4k", B=1, sq=4096, H=32, G=8, D=64, Tmax=4096, t_lo=4096,
+                 t_hi=4096, seed=_BASE_SEED + 22, note="fresh 4096-token prefill, D = 64"),
+    DecodeConfig("prefill_llama3_8b_8k", B=1, sq=8192, H=32, G=8, D=128, Tmax=8192, t_lo=8192,
+                 t_hi=8192, seed=_BASE_SEED + 23,
+                 note="fresh 8192-token prefill, Llama-3-8B-shaped layer"),
+    DecodeConfig("chunked_prefill_llama3_8b", B=4, sq=2048, H=32, G=8, D=128, Tmax=8192,
+                 t_lo=8192, t_hi=8192, seed=_BASE_SEED + 24,
+                 note="last 2048-token chunk of an 8192-token prompt, 4 sequences"),
+]
+
+
 def config_by_name(name: str) -> DecodeConfig:
-    for c in CONFIGS:
+    for c in CONFIGS + PREFILL_CONFIGS:
         if c.name == name:
             return c
     raise KeyError(name)

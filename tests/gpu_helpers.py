@@ -52,8 +52,8 @@ def min_tiles(n):
             os.environ["GQA_DECODE_MIN_TILES_PER_CTA"] = old
 
 
-def run_gpu(q, k, v, lens, scale, with_lse=True, device_inputs=None):
-    """Runs gqa_decode on the device. Returns (out float64 [B,sq,H,D], lse
+def run_gpu(q, k, v, lens, scale, with_lse=True, device_inputs=None, entry=None):
+    """Runs gqa_decode (or `entry`, a binding with its signature) on the device. Returns (out float64 [B,sq,H,D], lse
     float64 [B,sq,H] or None). Checks that the guard words around out and lse
     are untouched and that no device-side wait expired."""
     if device_inputs is None:
@@ -71,7 +71,7 @@ def run_gpu(q, k, v, lens, scale, with_lse=True, device_inputs=None):
         m = B * sq * H
         lse_buf = torch.full((m + 2 * _PAD,), float(_CANARY_F32), dtype=torch.float32, device="cuda")
         lse = lse_buf[_PAD:_PAD + m].view(B, sq, H)
-    gq.gqa_decode(dq, dk, dv, dl, scale, out, lse)
+    (entry or gq.gqa_decode)(dq, dk, dv, dl, scale, out, lse)
     torch.cuda.synchronize()
     assert gq.gqa_decode_check_error() == gq.GQA_OK
     ob = out_buf.cpu().numpy().view(np.uint16)

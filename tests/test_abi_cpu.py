@@ -16,13 +16,14 @@ HEADER = os.path.join(ROOT, "include", "gqa_decode.h")
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(gqa_decode\w*)\s*\(", src, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(gqa_\w+)\s*\(", src, flags=re.M)))
 
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("gqa_decode", "gqa_decode_ex", "gqa_decode_workspace_bytes", "gqa_decode_plan",
-              "gqa_decode_check_error", "gqa_decode_last_cuda_error", "gqa_decode_strerror"):
+              "gqa_decode_check_error", "gqa_decode_last_cuda_error", "gqa_decode_strerror",
+              "gqa_prefill"):
         assert n in names
 
 
@@ -86,3 +87,20 @@ def test_argument_checks_need_no_gpu():
     rc = lib.gqa_decode_ex(256, 520, 768, 1024, 0.1, 1280, None, 1, 1, 32, 8, 128, 64, 4096,
                            1 << 20, None)
     assert rc == gq.GQA_ERR_MISALIGNED
+
+
+def test_prefill_argument_checks_need_no_gpu():
+    lib = gq.load()
+    good = (256, 512, 768, 1024, 1280)
+
+    def call(ptrs, shape):
+        q, k, v, lens, out = ptrs
+        return lib.gqa_prefill(q, k, v, lens, 0.125, out, None, *shape, None)
+
+    assert call((None, 512, 768, 1024, 1280), (1, 64, 32, 8, 64, 4096)) == gq.GQA_ERR_INVALID_ARG
+    assert call(good, (1, 0, 32, 8, 64, 4096)) == gq.GQA_ERR_INVALID_ARG
+    assert call(good, (1, 64, 32, 6, 64, 4096)) == gq.GQA_ERR_HEAD_RATIO
+    assert call(good, (1, 64, 32, 8, 96, 4096)) == gq.GQA_ERR_UNSUPPORTED
+    assert call((256, 520, 768, 1024, 1280), (1, 64, 32, 8, 64, 4096)) == gq.GQA_ERR_MISALIGNED
+    # 2^31 rows of output would overflow the kernel's 32-bit row numbers
+    assert call(good, (1 << 16, 1 << 10, 32, 8, 64, 4096)) == gq.GQA_ERR_UNSUPPORTED
