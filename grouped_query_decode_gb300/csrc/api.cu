@@ -402,6 +402,7 @@ int gqa_prefill(const void* q, const void* k_cache, const void* v_cache, const i
                 float scale, void* out, float* lse, int B, int sq, int H, int G, int D, int Tmax,
                 cudaStream_t stream) {
     if (B <= 0 || sq <= 0 || H <= 0 || G <= 0 || D <= 0 || Tmax <= 0) return GQA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || scale > 3.0e38f) return GQA_ERR_INVALID_ARG;   // the row max is taken before scaling
     if (H % G != 0) return GQA_ERR_HEAD_RATIO;
     if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
     if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_INVALID_ARG;

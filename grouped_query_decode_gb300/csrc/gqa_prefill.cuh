@@ -284,36 +284,41 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
             }
             tc_fence_after();
             float x[kPfTokens];
+            {
+                uint32_t u[kPfTokens];
+                tmem_ld128(lane_addr + (j & 1) * kPfTokens, u);
 #pragma unroll
-            for (int c = 0; c < kPfTokens / 32; ++c) {
-                uint32_t u[32];
-                tmem_ld32(lane_addr + (j & 1) * kPfTokens + c * 32, u);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(u[i]);
+                for (int i = 0; i < kPfTokens; ++i) x[i] = __uint_as_float(u[i]);
             }
+            // Invisible keys -> -inf (only tiles that reach past this row's
+            // limit). The max is taken on the raw scores (scale > 0) with eight
+            // independent partial maxima and sums, so that no dependency chain
+            // runs the length of the row.
             const int t0 = j * kPfTokens;
-            if (t0 + kPfTokens - 1 <= lim) {
+            if (t0 + kPfTokens - 1 > lim) {
 #pragma unroll
-                for (int i = 0; i < kPfTokens; ++i) x[i] *= p.scale_log2;
-            } else {
-#pragma unroll
-                for (int i = 0; i < kPfTokens; ++i) x[i] = (t0 + i <= lim) ? x[i] * p.scale_log2 : -INFINITY;
+                for (int i = 0; i < kPfTokens; ++i) x[i] = (t0 + i <= lim) ? x[i] : -INFINITY;
             }
-            float mx = x[0];
+            float pm[8];
 #pragma unroll
-            for (int i = 1; i < kPfTokens; ++i) mx = fmaxf(mx, x[i]);
+            for (int k = 0; k < 8; ++k) pm[k] = x[k];
+#pragma unroll
+            for (int i = 8; i < kPfTokens; ++i) pm[i & 7] = fmaxf(pm[i & 7], x[i]);
+            const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * p.scale_log2;
             // The running max moves only when a score exceeds it by more than
             // kRescaleSlack (base 2); until then p <= 2^kRescaleSlack and the
             // O/l rescale is skipped. O, l and m stay consistent either way.
             const bool up = mx > m + kRescaleSlack;
             const float mn = up ? mx : m;
             const float base_m = mn == -INFINITY ? 0.f : mn;
-            float sum = 0.f;
+            float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int i = 0; i < kPfTokens; ++i) {
-                x[i] = fast_exp2(x[i] - base_m);
-                sum += x[i];
+                x[i] = fast_exp2(fmaf(x[i], p.scale_log2, -base_m));
+                ps[i & 7] += x[i];
             }
+            const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             if (j > 0) {
                 // P_{j-1} V_{j-1} has completed: the P buffer is free and O is
                 // settled for the rescale.

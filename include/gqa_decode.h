@@ -156,7 +156,8 @@ int gqa_decode_fp8(const void* q, const void* k_codes, const void* v_codes, cons
  * rows at once, and each row keeps its own causal limit and softmax. Same
  * arguments, layouts, causal rule (new token s at position T_b - sq + s sees
  * keys t <= T_b - sq + s), outputs and error codes as gqa_decode, with no
- * bound on (H/G) * sq; D in {64, 128}. A fresh prefill has T_b = sq; a
+ * bound on (H/G) * sq; D in {64, 128}; scale must be finite and > 0
+ * (GQA_ERR_INVALID_ARG otherwise). A fresh prefill has T_b = sq; a
  * chunked prefill has the earlier chunks' K/V in the cache as well.
  *
  * The products run on the tcgen05 tensor cores (bf16 inputs, fp32

@@ -99,6 +99,8 @@ def test_prefill_argument_checks_need_no_gpu():
 
     assert call((None, 512, 768, 1024, 1280), (1, 64, 32, 8, 64, 4096)) == gq.GQA_ERR_INVALID_ARG
     assert call(good, (1, 0, 32, 8, 64, 4096)) == gq.GQA_ERR_INVALID_ARG
+    assert lib.gqa_prefill(*good[:4], -0.125, good[4], None, 1, 64, 32, 8, 64, 4096, None) == \
+        gq.GQA_ERR_INVALID_ARG
     assert call(good, (1, 64, 32, 6, 64, 4096)) == gq.GQA_ERR_HEAD_RATIO
     assert call(good, (1, 64, 32, 8, 96, 4096)) == gq.GQA_ERR_UNSUPPORTED
     assert call((256, 520, 768, 1024, 1280), (1, 64, 32, 8, 64, 4096)) == gq.GQA_ERR_MISALIGNED
