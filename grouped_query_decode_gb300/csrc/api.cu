@@ -437,7 +437,7 @@ int gqa_prefill(const void* q, const void* k_cache, const void* v_cache, const i
     a.p.heads_per_group = H / G;
     a.p.row_tiles = (int)row_tiles;
     debug_knobs(&a.p.wait_timeout_ns, &a.p.skip_tile);
-    a.grid = (unsigned)((long long)B * G * row_tiles);
+    a.grid = (unsigned)((long long)B * G * ((row_tiles + 1) / 2));   // pairs of row tiles
     a.stream = stream;
     cudaError_t e = launch_prefill(D, a);
     if (e != cudaSuccess) return cuda_fail(e);

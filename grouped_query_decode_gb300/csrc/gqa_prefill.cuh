@@ -11,17 +11,22 @@
 // r = s * (H/G) + j for head j of the group), which keeps the causal limit of
 // a 128-row tile within a narrow band; the order is internal.
 //
-// One CTA per 128-row tile of one (b, g) unit. Warps 0-3 own one row each per
-// thread (TMEM lane = row): they stage Q, turn each 128x128 score tile S into
-// probabilities P (base-2 online softmax, lazy rescale of the O accumulator),
-// and write the output. Warp 4 streams 128-token K and V tiles with TMA into
-// 128-byte-swizzled shared memory. Warp 5 allocates tensor memory and one of
-// its threads issues the MMAs:
-//     S_j  = Q K_j^T        M = 128, N = 128, K = D   (TMEM, two buffers)
-//     O   += P_j V_j        M = 128, N = D,   K = 128 (TMEM)
-// S_{j+1} is computed while the softmax warps work on S_j. Every wait is
-// bounded; on expiry the CTA records the failure, lets its copies and MMAs
-// finish, frees its tensor memory and returns.
+// One CTA per pair of adjacent 128-row tiles (A, B) of one (b, g) unit; both
+// tiles use every 128-token K/V tile the CTA loads. Warpgroup 0 (warps 0-3)
+// runs tile A's softmax and epilogue, warpgroup 1 (warps 4-7) tile B's, one
+// thread per row (TMEM lane = row). Warp 8 streams K and V tiles with TMA into
+// 128-byte-swizzled shared memory; warp 9 allocates tensor memory and one of
+// its threads issues the MMAs, alternating between the two tiles so that the
+// tensor cores work on one tile while the other tile's softmax runs:
+//     S_X(j)  = Q_X K_j^T    M = 128, N = 128, K = D    (TMEM, fp32)
+//     O_X    += P_X(j) V_j   M = 128, N = D,   K = 128  (A = P in TMEM)
+// P_X(j) (bf16) is written over the first half of S_X(j)'s columns. The MMAs
+// of one thread execute in issue order, so S_X(j+1), issued after
+// P_X(j) V_j, does not overwrite P_X(j) before that product has read it; and
+// the commit that reports S_X(j+1) also reports P_X(j) V_j complete, which is
+// what the softmax needs before it rescales O_X. Every wait is bounded; on
+// expiry the CTA records the failure, lets its copies and MMAs finish, frees
+// its tensor memory and returns.
 #pragma once
 
 #include <cstdint>
@@ -40,16 +45,18 @@ template <int D>
 struct PrefillShape {
     static constexpr int kBlockBytes = 128 * 128;        // 128 rows x 128 B, 128-byte swizzle
     static constexpr int kDBlocks = D / 64;              // 64 bf16 columns per block
-    static constexpr int kQBytes = kDBlocks * kBlockBytes;
-    static constexpr int kPBytes = 2 * kBlockBytes;      // 128 rows x 128 tokens
+    static constexpr int kQBytes = kDBlocks * kBlockBytes;      // one Q tile
     static constexpr int kTileBytes = kDBlocks * kBlockBytes;   // one K (or V) tile
-    static constexpr int kStages = D == 128 ? 2 : 3;
-    static constexpr int kThreads = 6 * 32;
-    static constexpr int kBars = 4 * kStages + 6;
-    static constexpr int kSmemBytes =
-        1024 + kQBytes + kPBytes + 2 * kStages * kTileBytes + 8 * kBars + 16;
-    static constexpr uint32_t kTmemCols = 512;           // S0 | S1 | O
-    static constexpr uint32_t kColO = 256;
+    static constexpr int kStages = D == 128 ? 2 : 4;
+    static constexpr int kThreads = 10 * 32;
+    // k_full, k_empty, v_full, v_empty rings; per tile q_full, s_full,
+    // p_full, o_done; fin.
+    static constexpr int kBars = 4 * kStages + 8 + 1;
+    static constexpr int kSmemBytes = 1024 + 2 * kQBytes + 2 * kStages * kTileBytes + 8 * kBars + 16;
+    static constexpr uint32_t kTmemCols = 512;
+    // Columns: S_A | S_B | O_A | O_B.
+    static constexpr uint32_t kColS0 = 0, kColS1 = 128;
+    static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
 };
 
 // Lane 0 waits (bounded) and the warp agrees on the outcome.
@@ -71,15 +78,17 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t q_s = base;
-    const uint32_t p_s = q_s + PS::kQBytes;
-    const uint32_t k_s = p_s + PS::kPBytes;
+    const uint32_t q_s = base;                               // [2] Q tiles
+    const uint32_t k_s = q_s + 2 * PS::kQBytes;
     const uint32_t v_s = k_s + S * PS::kTileBytes;
     const uint32_t bar0 = v_s + S * PS::kTileBytes;
     const uint32_t k_full = bar0, k_empty = bar0 + 8 * S;
     const uint32_t v_full = bar0 + 16 * S, v_empty = bar0 + 24 * S;
-    const uint32_t s_full = bar0 + 32 * S;         // [2]
-    const uint32_t q_full = s_full + 16, p_full = q_full + 8, o_done = p_full + 8, fin = o_done + 8;
+    const uint32_t q_full = bar0 + 32 * S;                   // [2]
+    const uint32_t s_full = q_full + 16;                     // [2]
+    const uint32_t p_full = s_full + 16;                     // [2]
+    const uint32_t o_done = p_full + 16;                     // [2]
+    const uint32_t fin = o_done + 16;
     unsigned char* gen = smem_raw + (bar0 + 8 * PS::kBars - raw);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gen);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gen + 4);
@@ -88,18 +97,24 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
     const int lane = threadIdx.x & 31;
     const uint64_t tmo = p.wait_timeout_ns;
 
-    // Work item: the latest row tiles (most keys) first.
+    // Work item: a pair of row tiles, the latest pairs (most keys) first.
     const int units = p.B * p.G;
-    const int mt = p.row_tiles - 1 - (int)(blockIdx.x / units);
+    const int pairs = (p.row_tiles + 1) / 2;
+    const int pr = pairs - 1 - (int)(blockIdx.x / units);
     const int unit = (int)(blockIdx.x % units);
     const int b = unit / p.G, g = unit % p.G;
     const int tb = clamp_len(__ldg(p.seq_lens + b), p.Tmax);
-    const int r0 = mt * kPfRows;
-    const int rows = min(kPfRows, p.R - r0);
     const int hpg = p.heads_per_group;
-    // Token-major rows: the tile's last row has the largest causal limit.
-    const int lim_last = tb - p.sq + (r0 + rows - 1) / hpg;
-    const int nkv = lim_last < 0 ? 0 : lim_last / kPfTokens + 1;
+    int rows[2], nkv[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        const int r0 = (2 * pr + x) * kPfRows;
+        rows[x] = max(0, min(kPfRows, p.R - r0));
+        // Token-major rows: a tile's last row has the largest causal limit.
+        const int lim_last = rows[x] > 0 ? tb - p.sq + (r0 + rows[x] - 1) / hpg : -1;
+        nkv[x] = lim_last < 0 ? 0 : lim_last / kPfTokens + 1;
+    }
+    const int n_all = max(nkv[0], nkv[1]);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -108,20 +123,21 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
             mbar_init(v_full + 8 * s, 1);
             mbar_init(v_empty + 8 * s, 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(s_full + 8, 1);
-        mbar_init(q_full, kPfRows);
-        mbar_init(p_full, kPfRows);
-        mbar_init(o_done, 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(q_full + 8 * x, kPfRows);
+            mbar_init(s_full + 8 * x, 1);
+            mbar_init(p_full + 8 * x, kPfRows);
+            mbar_init(o_done + 8 * x, 1);
+        }
         mbar_init(fin, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(smem_addr(tmem_slot), PS::kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == 8 && lane == 0) {
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
     }
@@ -130,11 +146,11 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
             int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < nkv; ++j) {
+            for (int j = 0; j < n_all; ++j) {
                 const int s = j % S;
                 const uint32_t ph = ((j / S) & 1) ^ 1;
                 if (!wait_phase(k_empty + 8 * s, ph, abort_flag, p.status, tmo)) break;
@@ -168,51 +184,46 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
                     if (global_timer_ns() - t0 > tmo) break;
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------- MMA issuer
         constexpr uint32_t kIdescS = idesc_bf16_f32(kPfRows, kPfTokens, false, false);
         constexpr uint32_t kIdescO = idesc_bf16_f32(kPfRows, D, false, true);
-        auto issue_s = [&](int j) {
+        auto issue_s = [&](int x, int j) {
             const uint32_t kst = k_s + (j % S) * PS::kTileBytes;
+            const uint32_t qst = q_s + x * PS::kQBytes;
+            const uint32_t dst = tmem + (x ? PS::kColS1 : PS::kColS0);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * kBlock + (kk & 3) * 32;
-                umma_bf16(tmem + (j & 1) * kPfTokens, smem_desc_sw128(q_s + off, 16, 1024),
-                          smem_desc_sw128(kst + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                umma_bf16(dst, smem_desc_sw128(qst + off, 16, 1024), smem_desc_sw128(kst + off, 16, 1024),
+                          kIdescS, kk > 0 ? 1u : 0u);
             }
         };
-        auto issue_pv = [&](int j) {
+        auto issue_pv = [&](int x, int j) {
             const uint32_t vst = v_s + (j % S) * PS::kTileBytes;
+            const uint32_t pa = tmem + (x ? PS::kColS1 : PS::kColS0);
+            const uint32_t dst = tmem + (x ? PS::kColO1 : PS::kColO0);
 #pragma unroll
-            for (int kk = 0; kk < kPfTokens / 16; ++kk) {
-                const uint32_t a_off = (kk >> 2) * kBlock + (kk & 3) * 32;
-                umma_bf16(tmem + PS::kColO, smem_desc_sw128(p_s + a_off, 16, 1024),
-                          smem_desc_sw128(vst + kk * 16 * 128, kBlock, 1024), kIdescO,
-                          (j > 0 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < kPfTokens / 16; ++kk)
+                umma_bf16_ts(dst, pa + kk * 8, smem_desc_sw128(vst + kk * 16 * 128, kBlock, 1024), kIdescO,
+                             (j > 0 || kk > 0) ? 1u : 0u);
         };
-        bool ok = nkv > 0 && warp_wait(q_full, 0, abort_flag, p.status, tmo);
+        bool ok = n_all > 0;
+        for (int x = 0; ok && x < 2; ++x)
+            if (nkv[x] > 0) ok = warp_wait(q_full + 8 * x, 0, abort_flag, p.status, tmo);
         if (ok) ok = warp_wait(k_full, 0, abort_flag, p.status, tmo);
         const bool issued_any = ok;
         if (ok && lane == 0) {
             tc_fence_after();
-            issue_s(0);
-            umma_commit(s_full);
-            umma_commit(k_empty);
+            for (int x = 0; x < 2; ++x)
+                if (nkv[x] > 0) {
+                    issue_s(x, 0);
+                    umma_commit(s_full + 8 * x);
+                }
+            umma_commit(k_empty);   // K_0 is free once both S(0) have run
         }
         __syncwarp();
-        for (int j = 0; ok && j < nkv; ++j) {
-            if (j + 1 < nkv) {
-                const int s1 = (j + 1) % S;
-                ok = warp_wait(k_full + 8 * s1, ((j + 1) / S) & 1, abort_flag, p.status, tmo);
-                if (!ok) break;
-                if (lane == 0) {
-                    issue_s(j + 1);
-                    umma_commit(s_full + 8 * ((j + 1) & 1));
-                    umma_commit(k_empty + 8 * s1);
-                }
-                __syncwarp();
-            }
+        for (int j = 0; ok && j < n_all; ++j) {
             const int sv = j % S;
             ok = warp_wait(v_full + 8 * sv, (j / S) & 1, abort_flag, p.status, tmo);
             if (!ok) break;
@@ -230,12 +241,36 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            ok = warp_wait(p_full, j & 1, abort_flag, p.status, tmo);
+            bool k_ready = false;
+            for (int x = 0; ok && x < 2; ++x) {
+                if (j >= nkv[x]) continue;
+                ok = warp_wait(p_full + 8 * x, j & 1, abort_flag, p.status, tmo);
+                if (!ok) break;
+                if (lane == 0) {
+                    tc_fence_after();
+                    issue_pv(x, j);
+                }
+                if (j + 1 < nkv[x]) {
+                    if (!k_ready) {
+                        ok = warp_wait(k_full + 8 * ((j + 1) % S), ((j + 1) / S) & 1, abort_flag, p.status, tmo);
+                        if (!ok) break;
+                        k_ready = true;
+                    }
+                    if (lane == 0) {
+                        issue_s(x, j + 1);
+                        umma_commit(s_full + 8 * x);
+                    }
+                } else if (lane == 0) {
+                    umma_commit(o_done + 8 * x);
+                }
+                __syncwarp();
+            }
             if (!ok) break;
+            // K_{j+1} has had its last reader (S(j+1) of each tile) issued,
+            // V_j likewise (P(j) V_j): their stages are free once those MMAs
+            // complete.
             if (lane == 0) {
-                tc_fence_after();
-                issue_pv(j);
-                umma_commit(o_done);
+                if (k_ready) umma_commit(k_empty + 8 * ((j + 1) % S));
                 umma_commit(v_empty + 8 * sv);
             }
             __syncwarp();
@@ -253,42 +288,48 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------- softmax and epilogue warps
-        const int row = threadIdx.x;                  // 0..127 = TMEM lane
-        const int r = r0 + row;
-        const bool valid = row < rows;
+        const int x = warp >> 2;                      // tile A (0) or B (1)
+        const int row = threadIdx.x & 127;            // TMEM lane
+        const int r = (2 * pr + x) * kPfRows + row;
+        const bool valid = row < rows[x];
         const int s_tok = valid ? r / hpg : 0;
         const int jh = valid ? r % hpg : 0;
         const int lim = valid ? tb - p.sq + s_tok : -1;   // last visible key
         const size_t orow = ((size_t)(b * p.sq + s_tok) * p.H + (size_t)g * hpg + jh);
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t col_s = x ? PS::kColS1 : PS::kColS0;
+        const uint32_t col_o = x ? PS::kColO1 : PS::kColO0;
+        const int n = nkv[x];
 
         // Q row -> shared memory, K-major with the 128-byte swizzle.
-        {
+        if (n > 0) {
             const uint4* src = reinterpret_cast<const uint4*>(p.q + orow * D);
+            const uint32_t qst = q_s + x * PS::kQBytes;
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) {
                 const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-                st_shared_v4(q_s + (c >> 3) * kBlock + row * 128 + (((c & 7) ^ (row & 7)) << 4), v);
+                st_shared_v4(qst + (c >> 3) * kBlock + row * 128 + (((c & 7) ^ (row & 7)) << 4), v);
             }
             fence_proxy_async_smem();
-            mbar_arrive(q_full);
+            mbar_arrive(q_full + 8 * x);
         }
 
         float m = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < nkv; ++j) {
-            ok = wait_phase(s_full + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.status, tmo);
+        for (int j = 0; j < n; ++j) {
+            // S_X(j) is ready, and with it every earlier MMA (P_X(j-1) V_{j-1}).
+            ok = wait_phase(s_full + 8 * x, j & 1, abort_flag, p.status, tmo);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float x[kPfTokens];
+            float xs[kPfTokens];
             {
                 uint32_t u[kPfTokens];
-                tmem_ld128(lane_addr + (j & 1) * kPfTokens, u);
+                tmem_ld128(lane_addr + col_s, u);
 #pragma unroll
-                for (int i = 0; i < kPfTokens; ++i) x[i] = __uint_as_float(u[i]);
+                for (int i = 0; i < kPfTokens; ++i) xs[i] = __uint_as_float(u[i]);
             }
             // Invisible keys -> -inf (only tiles that reach past this row's
             // limit). The max is taken on the raw scores (scale > 0) with eight
@@ -297,13 +338,13 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
             const int t0 = j * kPfTokens;
             if (t0 + kPfTokens - 1 > lim) {
 #pragma unroll
-                for (int i = 0; i < kPfTokens; ++i) x[i] = (t0 + i <= lim) ? x[i] : -INFINITY;
+                for (int i = 0; i < kPfTokens; ++i) xs[i] = (t0 + i <= lim) ? xs[i] : -INFINITY;
             }
             float pm[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) pm[k] = x[k];
+            for (int k = 0; k < 8; ++k) pm[k] = xs[k];
 #pragma unroll
-            for (int i = 8; i < kPfTokens; ++i) pm[i & 7] = fmaxf(pm[i & 7], x[i]);
+            for (int i = 8; i < kPfTokens; ++i) pm[i & 7] = fmaxf(pm[i & 7], xs[i]);
             const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                                    fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * p.scale_log2;
             // The running max moves only when a score exceeds it by more than
@@ -313,63 +354,51 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
             const float mn = up ? mx : m;
             const float base_m = mn == -INFINITY ? 0.f : mn;
             float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[kPfTokens / 2];
 #pragma unroll
-            for (int i = 0; i < kPfTokens; ++i) {
-                x[i] = fast_exp2(fmaf(x[i], p.scale_log2, -base_m));
-                ps[i & 7] += x[i];
+            for (int i = 0; i < kPfTokens; i += 2) {
+                const float e0 = fast_exp2(fmaf(xs[i], p.scale_log2, -base_m));
+                const float e1 = fast_exp2(fmaf(xs[i + 1], p.scale_log2, -base_m));
+                ps[i & 7] += e0;
+                ps[(i + 1) & 7] += e1;
+                pk[i / 2] = pack_bf16x2(e0, e1);
             }
             const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-            if (j > 0) {
-                // P_{j-1} V_{j-1} has completed: the P buffer is free and O is
-                // settled for the rescale.
-                ok = wait_phase(o_done, (j - 1) & 1, abort_flag, p.status, tmo);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, up)) {
-                    const float alpha = up ? fast_exp2(m - base_m) : 1.f;
+            if (j > 0 && __any_sync(0xffffffffu, up)) {
+                // O_X holds P_X(j-1) V_{j-1} already (see above): rescale it.
+                const float alpha = up ? fast_exp2(m - base_m) : 1.f;
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t u[32];
-                        tmem_ld32(lane_addr + PS::kColO + c * 32, u);
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t u[32];
+                    tmem_ld32(lane_addr + col_o + c * 32, u);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-                        tmem_st32(lane_addr + PS::kColO + c * 32, u);
-                    }
-                    tmem_st_wait();
+                    for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                    tmem_st32(lane_addr + col_o + c * 32, u);
                 }
             }
             if (up) l *= fast_exp2(m - base_m);
             m = mn;
             l += sum;
-            // P (bf16) -> shared memory, K-major (tokens) with the 128-byte swizzle.
-#pragma unroll
-            for (int c = 0; c < kPfTokens / 8; ++c) {
-                const uint4 v = make_uint4(pack_bf16x2(x[8 * c], x[8 * c + 1]), pack_bf16x2(x[8 * c + 2], x[8 * c + 3]),
-                                           pack_bf16x2(x[8 * c + 4], x[8 * c + 5]),
-                                           pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
-                st_shared_v4(p_s + (c >> 3) * kBlock + row * 128 + (((c & 7) ^ (row & 7)) << 4), v);
-            }
-            fence_proxy_async_smem();
+            // P (bf16 pairs) over the first 64 columns of S_X.
+            tmem_st64(lane_addr + col_s, pk);
+            tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(p_full);
+            mbar_arrive(p_full + 8 * x);
         }
-        if (ok && nkv > 0) {
-            ok = wait_phase(o_done, (nkv - 1) & 1, abort_flag, p.status, tmo);
+        if (ok && n > 0) {
+            ok = wait_phase(o_done + 8 * x, 0, abort_flag, p.status, tmo);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) tc_fence_after();
         }
-        if (ok) {
+        if (ok && rows[x] > 0) {
             // Epilogue: O / l -> bf16 out, lse = (m + log2 l) ln 2.
             const float inv = l > 0.f ? 1.f / l : 0.f;
             uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t u[32];
-                if (nkv > 0) {
-                    tmem_ld32(lane_addr + PS::kColO + c * 32, u);
+                if (n > 0) {
+                    tmem_ld32(lane_addr + col_o + c * 32, u);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) u[i] = 0u;
@@ -392,7 +421,7 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, PS::kTmemCols);
     }
