@@ -40,6 +40,7 @@ namespace gqa {
 
 constexpr int kPfRows = 128;     // query rows per tile (MMA M; one TMEM lane each)
 constexpr int kPfTokens = 128;   // keys per K/V tile
+constexpr int kPrefetchTiles = 6;  // K/V tiles requested into L2 ahead of their loads
 
 template <int D>
 struct PrefillShape {
@@ -48,10 +49,10 @@ struct PrefillShape {
     static constexpr int kQBytes = kDBlocks * kBlockBytes;      // one Q tile
     static constexpr int kTileBytes = kDBlocks * kBlockBytes;   // one K (or V) tile
     static constexpr int kStages = D == 128 ? 2 : 4;
-    static constexpr int kThreads = 10 * 32;
+    static constexpr int kThreads = 11 * 32;
     // k_full, k_empty, v_full, v_empty rings; per tile q_full, s_full,
-    // p_full, o_done; fin.
-    static constexpr int kBars = 4 * kStages + 8 + 1;
+    // p_full, o_done, fin.
+    static constexpr int kBars = 4 * kStages + 8 + 4;
     static constexpr int kSmemBytes = 1024 + 2 * kQBytes + 2 * kStages * kTileBytes + 8 * kBars + 16;
     static constexpr uint32_t kTmemCols = 512;
     // Columns: S_A | S_B | O_A | O_B.
@@ -88,7 +89,8 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
     const uint32_t s_full = q_full + 16;                     // [2]
     const uint32_t p_full = s_full + 16;                     // [2]
     const uint32_t o_done = p_full + 16;                     // [2]
-    const uint32_t fin = o_done + 16;
+    const uint32_t fin = o_done + 16;                        // [2]
+    const uint32_t tok = fin + 16;                           // [2] turn tokens of the MMA warps
     unsigned char* gen = smem_raw + (bar0 + 8 * PS::kBars - raw);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gen);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gen + 4);
@@ -105,23 +107,25 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
     const int b = unit / p.G, g = unit % p.G;
     const int tb = clamp_len(__ldg(p.seq_lens + b), p.Tmax);
     const int hpg = p.heads_per_group;
-    int rows[2], nkv[2];
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-        const int r0 = (2 * pr + x) * kPfRows;
-        rows[x] = max(0, min(kPfRows, p.R - r0));
+    // Rows and key tiles of tile A (x = 0) and B (x = 1), kept in registers
+    // (selected, never indexed at run time).
+    auto tile_rows = [&](int x) { return max(0, min(kPfRows, p.R - (2 * pr + x) * kPfRows)); };
+    auto tile_nkv = [&](int x) {
+        const int rx = tile_rows(x);
         // Token-major rows: a tile's last row has the largest causal limit.
-        const int lim_last = rows[x] > 0 ? tb - p.sq + (r0 + rows[x] - 1) / hpg : -1;
-        nkv[x] = lim_last < 0 ? 0 : lim_last / kPfTokens + 1;
-    }
-    const int n_all = max(nkv[0], nkv[1]);
+        const int lim_last = rx > 0 ? tb - p.sq + ((2 * pr + x) * kPfRows + rx - 1) / hpg : -1;
+        return lim_last < 0 ? 0 : lim_last / kPfTokens + 1;
+    };
+    const int rows0 = tile_rows(0), rows1 = tile_rows(1);
+    const int nkv0 = tile_nkv(0), nkv1 = tile_nkv(1);
+    const int n_all = max(nkv0, nkv1);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(k_full + 8 * s, 1);
-            mbar_init(k_empty + 8 * s, 1);
+            mbar_init(k_empty + 8 * s, 2);   // one release per MMA warp
             mbar_init(v_full + 8 * s, 1);
-            mbar_init(v_empty + 8 * s, 1);
+            mbar_init(v_empty + 8 * s, 2);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(q_full + 8 * x, kPfRows);
@@ -130,6 +134,9 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
             mbar_init(o_done + 8 * x, 1);
         }
         mbar_init(fin, 1);
+        mbar_init(fin + 8, 1);
+        mbar_init(tok, 1);
+        mbar_init(tok + 8, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -150,9 +157,24 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
             int k_issued = 0, v_issued = 0;
+            // The CTAs of one (b, g) unit read the same K/V tiles at about the
+            // same time; asking L2 for tiles a few steps ahead keeps those
+            // reads from waiting on DRAM together.
+            for (int j = 0; j < kPrefetchTiles && j < n_all; ++j)
+#pragma unroll
+                for (int bx = 0; bx < PS::kDBlocks; ++bx) {
+                    tma_prefetch_l2_3d(&tm_k, bx * 64, j * kPfTokens, unit);
+                    tma_prefetch_l2_3d(&tm_v, bx * 64, j * kPfTokens, unit);
+                }
             for (int j = 0; j < n_all; ++j) {
                 const int s = j % S;
                 const uint32_t ph = ((j / S) & 1) ^ 1;
+                if (j + kPrefetchTiles < n_all)
+#pragma unroll
+                    for (int bx = 0; bx < PS::kDBlocks; ++bx) {
+                        tma_prefetch_l2_3d(&tm_k, bx * 64, (j + kPrefetchTiles) * kPfTokens, unit);
+                        tma_prefetch_l2_3d(&tm_v, bx * 64, (j + kPrefetchTiles) * kPfTokens, unit);
+                    }
                 if (!wait_phase(k_empty + 8 * s, ph, abort_flag, p.status, tmo)) break;
                 if (!(blockIdx.x == 0 && j == p.skip_tile)) {   // injected fault: tile never loaded
                     mbar_arrive_expect_tx(k_full + 8 * s, PS::kTileBytes);
@@ -184,51 +206,86 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
                     if (global_timer_ns() - t0 > tmo) break;
             }
         }
-    } else if (warp == 9) {
-        // ------------------------------------------------------- MMA issuer
+    } else if (warp == 9 || warp == 10) {
+        // ------------------------------------- MMA issuers, one warp per tile
+        // Warp 9 serves tile A, warp 10 tile B, so that neither tile's
+        // products wait behind the other's. Each releases every K/V stage
+        // once; a stage is refilled after both have.
+        const int x = warp - 9;
+        const int nx = x ? nkv1 : nkv0;
         constexpr uint32_t kIdescS = idesc_bf16_f32(kPfRows, kPfTokens, false, false);
         constexpr uint32_t kIdescO = idesc_bf16_f32(kPfRows, D, false, true);
-        auto issue_s = [&](int x, int j) {
+        const uint32_t qst = q_s + x * PS::kQBytes;
+        const uint32_t s_tm = tmem + (x ? PS::kColS1 : PS::kColS0);
+        const uint32_t o_tm = tmem + (x ? PS::kColO1 : PS::kColO0);
+        auto issue_s = [&](int j) {
             const uint32_t kst = k_s + (j % S) * PS::kTileBytes;
-            const uint32_t qst = q_s + x * PS::kQBytes;
-            const uint32_t dst = tmem + (x ? PS::kColS1 : PS::kColS0);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * kBlock + (kk & 3) * 32;
-                umma_bf16(dst, smem_desc_sw128(qst + off, 16, 1024), smem_desc_sw128(kst + off, 16, 1024),
+                umma_bf16(s_tm, smem_desc_sw128(qst + off, 16, 1024), smem_desc_sw128(kst + off, 16, 1024),
                           kIdescS, kk > 0 ? 1u : 0u);
             }
+            umma_commit(s_full + 8 * x);
+            umma_commit(k_empty + 8 * (j % S));    // K_j has had its last reader from this tile
         };
-        auto issue_pv = [&](int x, int j) {
+        auto issue_pv = [&](int j) {
             const uint32_t vst = v_s + (j % S) * PS::kTileBytes;
-            const uint32_t pa = tmem + (x ? PS::kColS1 : PS::kColS0);
-            const uint32_t dst = tmem + (x ? PS::kColO1 : PS::kColO0);
 #pragma unroll
             for (int kk = 0; kk < kPfTokens / 16; ++kk)
-                umma_bf16_ts(dst, pa + kk * 8, smem_desc_sw128(vst + kk * 16 * 128, kBlock, 1024), kIdescO,
+                umma_bf16_ts(o_tm, s_tm + kk * 8, smem_desc_sw128(vst + kk * 16 * 128, kBlock, 1024), kIdescO,
                              (j > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(v_empty + 8 * (j % S));
         };
-        bool ok = n_all > 0;
-        for (int x = 0; ok && x < 2; ++x)
-            if (nkv[x] > 0) ok = warp_wait(q_full + 8 * x, 0, abort_flag, p.status, tmo);
-        if (ok) ok = warp_wait(k_full, 0, abort_flag, p.status, tmo);
-        const bool issued_any = ok;
-        if (ok && lane == 0) {
+        bool ok = true;
+        bool issued_any = false;
+        // The two warps take turns: A issues S_A(0), then B S_B(0), then A
+        // its batch {P_A(0) V_0, S_A(1)}, then B its batch, and so on; turn
+        // k of warp x is arrival k on tok[x], which the other warp waits for
+        // before its own turn. Each tile's softmax then runs while the
+        // tensor cores work through the other tile's batch.
+        uint32_t turn = 0;                     // turns this warp has taken
+        auto my_turn = [&]() {
+            // A's turn t follows B's turn t-1; B's turn t follows A's turn t.
+            if (x == 0 && turn == 0) return true;
+            const uint32_t k = x == 0 ? turn - 1 : turn;
+            return warp_wait(tok + 8 * (1 - x), k & 1, abort_flag, p.status, tmo);
+        };
+        auto end_turn = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tok + 8 * x);
+            ++turn;
+        };
+        if (nx > 0) ok = warp_wait(q_full + 8 * x, 0, abort_flag, p.status, tmo) &&
+                         warp_wait(k_full, 0, abort_flag, p.status, tmo);
+        if (ok) ok = my_turn();
+        if (ok && nx > 0 && lane == 0) {
             tc_fence_after();
-            for (int x = 0; x < 2; ++x)
-                if (nkv[x] > 0) {
-                    issue_s(x, 0);
-                    umma_commit(s_full + 8 * x);
-                }
-            umma_commit(k_empty);   // K_0 is free once both S(0) have run
+            issue_s(0);
         }
-        __syncwarp();
+        issued_any = ok && nx > 0;
+        if (ok) end_turn();
         for (int j = 0; ok && j < n_all; ++j) {
             const int sv = j % S;
-            ok = warp_wait(v_full + 8 * sv, (j / S) & 1, abort_flag, p.status, tmo);
+            const uint32_t ph = (j / S) & 1;
+            if (j >= nx) {
+                // A key tile only the other tile needs: release its stages
+                // once their copies have landed, and pass the turn.
+                ok = warp_wait(k_full + 8 * sv, ph, abort_flag, p.status, tmo) &&
+                     warp_wait(v_full + 8 * sv, ph, abort_flag, p.status, tmo) && my_turn();
+                if (ok && lane == 0) {
+                    mbar_arrive(k_empty + 8 * sv);
+                    mbar_arrive(v_empty + 8 * sv);
+                }
+                if (ok) end_turn();
+                continue;
+            }
+            ok = warp_wait(v_full + 8 * sv, ph, abort_flag, p.status, tmo);
             if (!ok) break;
             // Keys past the valid length may hold anything (NaN included);
-            // zero their V rows so that p = 0 times them stays 0.
+            // zero their V rows so that p = 0 times them stays 0. Both MMA
+            // warps may write the same zeros; each does so before its own
+            // product reads them.
             const int valid = tb - j * kPfTokens;
             if (valid < kPfTokens) {
                 const uint32_t vst = v_s + sv * PS::kTileBytes;
@@ -241,45 +298,26 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            bool k_ready = false;
-            for (int x = 0; ok && x < 2; ++x) {
-                if (j >= nkv[x]) continue;
-                ok = warp_wait(p_full + 8 * x, j & 1, abort_flag, p.status, tmo);
-                if (!ok) break;
-                if (lane == 0) {
-                    tc_fence_after();
-                    issue_pv(x, j);
-                }
-                if (j + 1 < nkv[x]) {
-                    if (!k_ready) {
-                        ok = warp_wait(k_full + 8 * ((j + 1) % S), ((j + 1) / S) & 1, abort_flag, p.status, tmo);
-                        if (!ok) break;
-                        k_ready = true;
-                    }
-                    if (lane == 0) {
-                        issue_s(x, j + 1);
-                        umma_commit(s_full + 8 * x);
-                    }
-                } else if (lane == 0) {
-                    umma_commit(o_done + 8 * x);
-                }
-                __syncwarp();
-            }
+            ok = warp_wait(p_full + 8 * x, j & 1, abort_flag, p.status, tmo);
+            if (ok && j + 1 < nx)
+                ok = warp_wait(k_full + 8 * ((j + 1) % S), ((j + 1) / S) & 1, abort_flag, p.status, tmo);
+            if (ok) ok = my_turn();
             if (!ok) break;
-            // K_{j+1} has had its last reader (S(j+1) of each tile) issued,
-            // V_j likewise (P(j) V_j): their stages are free once those MMAs
-            // complete.
             if (lane == 0) {
-                if (k_ready) umma_commit(k_empty + 8 * ((j + 1) % S));
-                umma_commit(v_empty + 8 * sv);
+                tc_fence_after();
+                issue_pv(j);
+                if (j + 1 < nx)
+                    issue_s(j + 1);   // after P(j) V_j, which reads the same columns
+                else
+                    umma_commit(o_done + 8 * x);
             }
-            __syncwarp();
+            end_turn();
         }
-        // Every MMA this thread issued has completed once `fin` flips.
+        // Every MMA this warp issued has completed once `fin` flips.
         if (issued_any && lane == 0) {
-            umma_commit(fin);
+            umma_commit(fin + 8 * x);
             const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(fin, 0))
+            while (!mbar_try_wait(fin + 8 * x, 0))
                 if (global_timer_ns() - t0 > tmo) {
                     atomicOr(p.status, kStatusTimeout);
                     break;
@@ -291,7 +329,8 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
         const int x = warp >> 2;                      // tile A (0) or B (1)
         const int row = threadIdx.x & 127;            // TMEM lane
         const int r = (2 * pr + x) * kPfRows + row;
-        const bool valid = row < rows[x];
+        const int rows_x = x ? rows1 : rows0;
+        const bool valid = row < rows_x;
         const int s_tok = valid ? r / hpg : 0;
         const int jh = valid ? r % hpg : 0;
         const int lim = valid ? tb - p.sq + s_tok : -1;   // last visible key
@@ -299,7 +338,7 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t col_s = x ? PS::kColS1 : PS::kColS0;
         const uint32_t col_o = x ? PS::kColO1 : PS::kColO0;
-        const int n = nkv[x];
+        const int n = x ? nkv1 : nkv0;
 
         // Q row -> shared memory, K-major with the 128-byte swizzle.
         if (n > 0) {
@@ -390,7 +429,7 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (ok) tc_fence_after();
         }
-        if (ok && rows[x] > 0) {
+        if (ok && rows_x > 0) {
             // Epilogue: O / l -> bf16 out, lse = (m + log2 l) ln 2.
             const float inv = l > 0.f ? 1.f / l : 0.f;
             uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
