@@ -381,11 +381,13 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
             }
             float pm[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) pm[k] = xs[k];
+            for (int k = 0; k < 8; ++k) pm[k] = fmaxf(xs[k], xs[k + 8]);
 #pragma unroll
-            for (int i = 8; i < kPfTokens; ++i) pm[i & 7] = fmaxf(pm[i & 7], xs[i]);
-            const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * p.scale_log2;
+            for (int i = 16; i < kPfTokens; i += 16)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) pm[k] = fmax3(pm[k], xs[i + k], xs[i + 8 + k]);
+            const float mx = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(fmax3(pm[3], pm[4], pm[5]), pm[6], pm[7])) *
+                             p.scale_log2;
             // The running max moves only when a score exceeds it by more than
             // kRescaleSlack (base 2); until then p <= 2^kRescaleSlack and the
             // O/l rescale is skipped. O, l and m stay consistent either way.
