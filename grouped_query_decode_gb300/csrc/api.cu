@@ -417,6 +417,30 @@ int gqa_prefill(const void* q, const void* k_cache, const void* v_cache, const i
     DeviceInfo info;
     int st = device_info(&info);
     if (st != GQA_OK) return st;
+    // Short chunks: when the pairs of row tiles cannot fill the SMs, each
+    // pair's key range is shared by several CTAs (at least two key tiles
+    // each) and a second kernel merges their partials.
+    const long long items = (long long)B * G * ((row_tiles + 1) / 2);
+    const long long key_tiles = (Tmax + 127) / 128;
+    long long splits = 1;
+    if (2 * items < info.sms) {
+        splits = (info.sms + items - 1) / items;
+        if (splits > key_tiles / 2) splits = key_tiles / 2;
+        if (splits < 1) splits = 1;
+    }
+    if (const char* f = std::getenv("GQA_PREFILL_SPLITS")) {   // sweeps and tests
+        const long long x = std::atoll(f);
+        if (x > 0) splits = x;
+    }
+    if (splits > 32) splits = 32;   // the combine keeps one split per lane
+    if (items * splits >= (1ll << 31)) return GQA_ERR_UNSUPPORTED;
+    void* ws = nullptr;
+    size_t have = 0;
+    const size_t need = prefill_workspace_bytes(D, items, (int)splits);
+    if (need > 0) {
+        st = stream_workspace(stream, need, &ws, &have);
+        if (st != GQA_OK) return st;
+    }
     PrefillLaunchArgs a{};
     st = encode_cache_map(&a.tm_k, k_cache, (long long)B * G, Tmax, D, 128);
     if (st != GQA_OK) return st;
@@ -437,7 +461,9 @@ int gqa_prefill(const void* q, const void* k_cache, const void* v_cache, const i
     a.p.heads_per_group = H / G;
     a.p.row_tiles = (int)row_tiles;
     debug_knobs(&a.p.wait_timeout_ns, &a.p.skip_tile);
-    a.grid = (unsigned)((long long)B * G * ((row_tiles + 1) / 2));   // pairs of row tiles
+    a.p.splits = (int)splits;
+    a.p.ws_part = static_cast<float*>(ws);
+    a.grid = (unsigned)(items * splits);   // (pair of row tiles, key range)
     a.stream = stream;
     cudaError_t e = launch_prefill(D, a);
     if (e != cudaSuccess) return cuda_fail(e);

@@ -80,6 +80,12 @@ struct PrefillParams {
     float scale_log2;
     int B, sq, H, G, Tmax, R, heads_per_group, row_tiles;
     int skip_tile;            // fault injection for tests (-1: off)
+    // Split key ranges (short chunks): each pair of row tiles is shared by
+    // `splits` CTAs over consecutive key ranges; with splits > 1 every CTA
+    // writes per-row partials (O/l, m, l) to `ws_part` instead of out/lse,
+    // and gqa_prefill_combine merges them.
+    int splits;
+    float* ws_part;           // [B*G][pairs][splits][2 tiles][128 rows][D + 4]: O, m, l, pad
 };
 
 // One CTA per SM. Every 16-row tile of the group has four consumer warps

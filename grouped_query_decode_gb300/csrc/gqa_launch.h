@@ -32,7 +32,8 @@ struct PrefillLaunchArgs {
     unsigned grid;
     cudaStream_t stream;
 };
-cudaError_t launch_prefill(int D, const PrefillLaunchArgs& a);
+cudaError_t launch_prefill(int D, const PrefillLaunchArgs& a);   // + the combine when split
+size_t prefill_workspace_bytes(int D, long long items, int splits);
 int prefill_smem_bytes(int D);
 
 // Dynamic shared memory and threads per CTA of the split-KV kernel.

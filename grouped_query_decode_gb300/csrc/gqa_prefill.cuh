@@ -41,6 +41,9 @@ namespace gqa {
 constexpr int kPfRows = 128;     // query rows per tile (MMA M; one TMEM lane each)
 constexpr int kPfTokens = 128;   // keys per K/V tile
 constexpr int kPrefetchTiles = 6;  // K/V tiles requested into L2 ahead of their loads
+// Floats per row of a split partial: O[D], m, l, padded so that every row
+// starts on a 16-byte boundary (the epilogue stores O with 16-byte stores).
+__host__ __device__ constexpr int prefill_part_stride(int D) { return D + 4; }
 
 template <int D>
 struct PrefillShape {
@@ -68,7 +71,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-template <int D>
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
     gqa_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -99,11 +102,14 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
     const int lane = threadIdx.x & 31;
     const uint64_t tmo = p.wait_timeout_ns;
 
-    // Work item: a pair of row tiles, the latest pairs (most keys) first.
+    // Work item: a pair of row tiles (the latest pairs, with the most keys,
+    // first) and, for short chunks, one of `splits` key ranges of it.
     const int units = p.B * p.G;
     const int pairs = (p.row_tiles + 1) / 2;
-    const int pr = pairs - 1 - (int)(blockIdx.x / units);
-    const int unit = (int)(blockIdx.x % units);
+    const int split = SPLIT ? (int)(blockIdx.x % p.splits) : 0;
+    const int item = SPLIT ? (int)(blockIdx.x / p.splits) : (int)blockIdx.x;
+    const int pr = pairs - 1 - item / units;
+    const int unit = item % units;
     const int b = unit / p.G, g = unit % p.G;
     const int tb = clamp_len(__ldg(p.seq_lens + b), p.Tmax);
     const int hpg = p.heads_per_group;
@@ -117,7 +123,13 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
         return lim_last < 0 ? 0 : lim_last / kPfTokens + 1;
     };
     const int rows0 = tile_rows(0), rows1 = tile_rows(1);
-    const int nkv0 = tile_nkv(0), nkv1 = tile_nkv(1);
+    // This CTA's key tiles [j0, j0 + n) of the pair; each tile's own count is
+    // cut to the keys it sees. Ring stages and phases count from j0.
+    const int n_pair = max(tile_nkv(0), tile_nkv(1));
+    const int j0 = SPLIT ? (int)((long long)split * n_pair / p.splits) : 0;
+    const int j1 = SPLIT ? (int)((long long)(split + 1) * n_pair / p.splits) : n_pair;
+    const int nkv0 = SPLIT ? max(0, min(tile_nkv(0), j1) - j0) : tile_nkv(0);
+    const int nkv1 = SPLIT ? max(0, min(tile_nkv(1), j1) - j0) : tile_nkv(1);
     const int n_all = max(nkv0, nkv1);
 
     if (threadIdx.x == 0) {
@@ -163,8 +175,8 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
             for (int j = 0; j < kPrefetchTiles && j < n_all; ++j)
 #pragma unroll
                 for (int bx = 0; bx < PS::kDBlocks; ++bx) {
-                    tma_prefetch_l2_3d(&tm_k, bx * 64, j * kPfTokens, unit);
-                    tma_prefetch_l2_3d(&tm_v, bx * 64, j * kPfTokens, unit);
+                    tma_prefetch_l2_3d(&tm_k, bx * 64, (j0 + j) * kPfTokens, unit);
+                    tma_prefetch_l2_3d(&tm_v, bx * 64, (j0 + j) * kPfTokens, unit);
                 }
             for (int j = 0; j < n_all; ++j) {
                 const int s = j % S;
@@ -172,8 +184,8 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
                 if (j + kPrefetchTiles < n_all)
 #pragma unroll
                     for (int bx = 0; bx < PS::kDBlocks; ++bx) {
-                        tma_prefetch_l2_3d(&tm_k, bx * 64, (j + kPrefetchTiles) * kPfTokens, unit);
-                        tma_prefetch_l2_3d(&tm_v, bx * 64, (j + kPrefetchTiles) * kPfTokens, unit);
+                        tma_prefetch_l2_3d(&tm_k, bx * 64, (j0 + j + kPrefetchTiles) * kPfTokens, unit);
+                        tma_prefetch_l2_3d(&tm_v, bx * 64, (j0 + j + kPrefetchTiles) * kPfTokens, unit);
                     }
                 if (!wait_phase(k_empty + 8 * s, ph, abort_flag, p.status, tmo)) break;
                 if (!(blockIdx.x == 0 && j == p.skip_tile)) {   // injected fault: tile never loaded
@@ -181,7 +193,7 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
 #pragma unroll
                     for (int bx = 0; bx < PS::kDBlocks; ++bx)
                         tma_load_3d(k_s + s * PS::kTileBytes + bx * kBlock, &tm_k, k_full + 8 * s, bx * 64,
-                                    j * kPfTokens, unit);
+                                    (j0 + j) * kPfTokens, unit);
                     k_issued = j + 1;
                 }
                 if (!wait_phase(v_empty + 8 * s, ph, abort_flag, p.status, tmo)) break;
@@ -189,7 +201,7 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
 #pragma unroll
                 for (int bx = 0; bx < PS::kDBlocks; ++bx)
                     tma_load_3d(v_s + s * PS::kTileBytes + bx * kBlock, &tm_v, v_full + 8 * s, bx * 64,
-                                j * kPfTokens, unit);
+                                (j0 + j) * kPfTokens, unit);
                 v_issued = j + 1;
             }
             // Leave only once the copies of the last tiles have landed (the
@@ -286,7 +298,7 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
             // zero their V rows so that p = 0 times them stays 0. Both MMA
             // warps may write the same zeros; each does so before its own
             // product reads them.
-            const int valid = tb - j * kPfTokens;
+            const int valid = tb - (j0 + j) * kPfTokens;
             if (valid < kPfTokens) {
                 const uint32_t vst = v_s + sv * PS::kTileBytes;
                 const int first = valid > 0 ? valid : 0;
@@ -332,9 +344,21 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
         const int rows_x = x ? rows1 : rows0;
         const bool valid = row < rows_x;
         const int s_tok = valid ? r / hpg : 0;
-        const int jh = valid ? r % hpg : 0;
         const int lim = valid ? tb - p.sq + s_tok : -1;   // last visible key
-        const size_t orow = ((size_t)(b * p.sq + s_tok) * p.H + (size_t)g * hpg + jh);
+        // Global row of (b, s_tok, head g*hpg + j); recomputed where needed
+        // from a fresh read of the CTA index so that it is not held in
+        // registers through the softmax loop.
+        auto out_row = [&](int& unit_o, int& pr_o, int& split_o) -> size_t {
+            uint32_t cta;
+            asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(cta));
+            split_o = SPLIT ? (int)(cta % p.splits) : 0;
+            const int it = SPLIT ? (int)(cta / p.splits) : (int)cta;
+            unit_o = it % units;
+            pr_o = pairs - 1 - it / units;
+            const int rr = (2 * pr_o + x) * kPfRows + row;
+            const int bo = unit_o / p.G, go = unit_o % p.G;
+            return (size_t)(bo * p.sq + rr / hpg) * p.H + (size_t)go * hpg + rr % hpg;
+        };
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t col_s = x ? PS::kColS1 : PS::kColS0;
         const uint32_t col_o = x ? PS::kColO1 : PS::kColO0;
@@ -342,7 +366,8 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
 
         // Q row -> shared memory, K-major with the 128-byte swizzle.
         if (n > 0) {
-            const uint4* src = reinterpret_cast<const uint4*>(p.q + orow * D);
+            int uo, po, so;
+            const uint4* src = reinterpret_cast<const uint4*>(p.q + out_row(uo, po, so) * D);
             const uint32_t qst = q_s + x * PS::kQBytes;
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) {
@@ -374,7 +399,7 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
             // limit). The max is taken on the raw scores (scale > 0) with eight
             // independent partial maxima and sums, so that no dependency chain
             // runs the length of the row.
-            const int t0 = j * kPfTokens;
+            const int t0 = (j0 + j) * kPfTokens;
             if (t0 + kPfTokens - 1 > lim) {
 #pragma unroll
                 for (int i = 0; i < kPfTokens; ++i) xs[i] = (t0 + i <= lim) ? xs[i] : -INFINITY;
@@ -432,9 +457,16 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
             if (ok) tc_fence_after();
         }
         if (ok && rows_x > 0) {
-            // Epilogue: O / l -> bf16 out, lse = (m + log2 l) ln 2.
+            // Epilogue: O / l -> bf16 out and lse = (m + log2 l) ln 2; or, for a
+            // split key range, the partial O / l (fp32), m (base 2) and l.
+            constexpr bool part = SPLIT;
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
+            int uo, po, so;
+            const size_t orow = out_row(uo, po, so);
+            uint16_t* dst = p.out + orow * D;
+            constexpr int kStride = prefill_part_stride(D);
+            float* slot = p.ws_part + ((((size_t)uo * pairs + po) * p.splits + so) * 2 + x) * kPfRows * kStride +
+                          (size_t)row * kStride;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t u[32];
@@ -444,19 +476,24 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) u[i] = 0u;
                 }
-                if (valid) {
+                if (!valid) continue;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = pack_bf16x2(__uint_as_float(u[8 * k + 2 * e]) * inv,
-                                               __uint_as_float(u[8 * k + 2 * e + 1]) * inv);
-                        dst[c * 4 + k] = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
+                for (int k = 0; k < 8; ++k) {
+                    const float f0 = __uint_as_float(u[4 * k]) * inv, f1 = __uint_as_float(u[4 * k + 1]) * inv;
+                    const float f2 = __uint_as_float(u[4 * k + 2]) * inv, f3 = __uint_as_float(u[4 * k + 3]) * inv;
+                    if (part)
+                        *reinterpret_cast<float4*>(slot + c * 32 + 4 * k) = make_float4(f0, f1, f2, f3);
+                    else
+                        *reinterpret_cast<uint2*>(dst + c * 32 + 4 * k) =
+                            make_uint2(pack_bf16x2(f0, f1), pack_bf16x2(f2, f3));
                 }
             }
-            if (valid && p.lse) p.lse[orow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            if (valid) {
+                if (part)
+                    *reinterpret_cast<float2*>(slot + D) = make_float2(l > 0.f ? m : -INFINITY, l);
+                else if (p.lse)
+                    p.lse[orow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            }
         }
     }
 
@@ -466,6 +503,76 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, PS::kTmemCols);
     }
+}
+
+// Merges the key-range partials of split prefill CTAs: per row
+// M = max_s m_s, L = sum_s l_s 2^(m_s - M), O = sum_s (O/l)_s l_s 2^(m_s - M) / L,
+// lse = (M + log2 L) ln 2. One warp per row: lane s holds split s's (m, l)
+// (splits <= 32), then the warp sums the O rows, four splits in flight, each
+// lane D/32 columns.
+template <int D>
+__global__ void __launch_bounds__(256) gqa_prefill_combine(const PrefillParams p) {
+    constexpr int kStride = prefill_part_stride(D);
+    constexpr int kPer = D / 32;
+    const int units = p.B * p.G;
+    const int pairs = (p.row_tiles + 1) / 2;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x / (kPfRows / 8);              // (item, x)
+    const int row = (blockIdx.x % (kPfRows / 8)) * 8 + warp;
+    const int x = tile & 1, item = tile >> 1;
+    const int pr = item / units, unit = item % units;
+    const int r0 = (2 * pr + x) * kPfRows;
+    if (row >= p.R - r0) return;
+    const int b = unit / p.G, g = unit % p.G;
+    const size_t slot_stride = (size_t)2 * kPfRows * kStride;
+    const float* base = p.ws_part + ((((size_t)unit * pairs + pr) * p.splits) * 2 + x) * kPfRows * kStride +
+                        (size_t)row * kStride;
+    float m = -INFINITY, l = 0.f;
+    if (lane < p.splits) {
+        const float2 ml = *reinterpret_cast<const float2*>(base + lane * slot_stride + D);
+        m = ml.x;
+        l = ml.y;
+    }
+    float M = m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float w = (l == 0.f || m == -INFINITY) ? 0.f : l * fast_exp2(m - M);
+    float L = w;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    float acc[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+    for (int s0 = 0; s0 < p.splits; s0 += 4) {
+        float v[4][kPer];
+        float ws[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            ws[u] = __shfl_sync(0xffffffffu, w, (s0 + u) & 31);
+            const bool use = s0 + u < p.splits && ws[u] != 0.f;
+            const float* src = base + (s0 + u) * slot_stride + lane * kPer;
+#pragma unroll
+            for (int i = 0; i < kPer; i += 2) {
+                const float2 t = use ? *reinterpret_cast<const float2*>(src + i) : make_float2(0.f, 0.f);
+                v[u][i] = t.x;
+                v[u][i + 1] = t.y;
+            }
+            if (!use) ws[u] = 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) acc[i] += ws[u] * v[u][i];
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int r = r0 + row;
+    const size_t orow = (size_t)(b * p.sq + r / p.heads_per_group) * p.H + (size_t)g * p.heads_per_group +
+                        r % p.heads_per_group;
+    uint16_t* dst = p.out + orow * D + lane * kPer;
+#pragma unroll
+    for (int i = 0; i < kPer; i += 2)
+        *reinterpret_cast<uint32_t*>(dst + i) = pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
+    if (lane == 0 && p.lse) p.lse[orow] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
 }  // namespace gqa

@@ -8,7 +8,7 @@ namespace gqa {
 
 namespace {
 
-template <int D>
+template <int D, bool SPLIT>
 cudaError_t launch_prefill_t(const PrefillLaunchArgs& a) {
     using PS = PrefillShape<D>;
     // The shared-memory opt-in is per function and per device.
@@ -18,19 +18,28 @@ cudaError_t launch_prefill_t(const PrefillLaunchArgs& a) {
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(attr_set_mask.load() & bit)) {
-        e = cudaFuncSetAttribute(gqa_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(gqa_prefill_kernel<D, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PS::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set_mask.fetch_or(bit);
     }
-    gqa_prefill_kernel<D><<<a.grid, PS::kThreads, PS::kSmemBytes, a.stream>>>(a.tm_k, a.tm_v, a.p);
+    gqa_prefill_kernel<D, SPLIT><<<a.grid, PS::kThreads, PS::kSmemBytes, a.stream>>>(a.tm_k, a.tm_v, a.p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || !SPLIT) return e;
+    // One warp per row: (items x 2 tiles) x 16 CTAs of 8 warps.
+    gqa_prefill_combine<D><<<a.grid / a.p.splits * 2 * (kPfRows / 8), 256, 0, a.stream>>>(a.p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(int D, const PrefillLaunchArgs& a) {
-    return D == 64 ? launch_prefill_t<64>(a) : launch_prefill_t<128>(a);
+    if (a.p.splits > 1) return D == 64 ? launch_prefill_t<64, true>(a) : launch_prefill_t<128, true>(a);
+    return D == 64 ? launch_prefill_t<64, false>(a) : launch_prefill_t<128, false>(a);
+}
+
+size_t prefill_workspace_bytes(int D, long long items, int splits) {
+    return splits <= 1 ? 0 : sizeof(float) * (size_t)items * splits * 2 * kPfRows * prefill_part_stride(D);
 }
 
 int prefill_smem_bytes(int D) { return D == 64 ? PrefillShape<64>::kSmemBytes : PrefillShape<128>::kSmemBytes; }

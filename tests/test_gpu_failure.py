@@ -39,3 +39,31 @@ def test_expired_wait_is_reported_and_the_context_survives(monkeypatch, H, G, sq
     ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, 1 / math.sqrt(D), threads=8)
     got_out, got_lse = run_gpu(q, k, v, lens, 1 / math.sqrt(D), device_inputs=(dq, dk, dv, dl))
     compare(got_out, got_lse, ref_out, ref_lse, what="after timeout")
+
+
+def test_prefill_expired_wait_is_reported_and_the_context_survives(monkeypatch):
+    """The tcgen05 prefill kernel on the same hook: CTA 0's MMA warps wait for a
+    K tile that never comes, give up, let the products they issued finish, and
+    the CTA frees its tensor memory before returning (a later launch on that SM
+    allocates it again). The next call, without the hook, matches the oracle."""
+    B, sq, H, G, D, Tmax = 1, 300, 8, 2, 128, 700
+    q, k, v, lens = make_inputs(B, sq, H, G, D, Tmax, [700], seed=91)
+    dq, dk, dv = to_device_bf16(q), to_device_bf16(k), to_device_bf16(v)
+    dl = torch.from_numpy(lens).cuda()
+    out = torch.empty(B, sq, H, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, sq, H, dtype=torch.float32, device="cuda")
+    assert gq.gqa_decode_check_error() == gq.GQA_OK
+
+    monkeypatch.setenv("GQA_DECODE_DEBUG_TIMEOUT_MS", "200")
+    monkeypatch.setenv("GQA_DECODE_DEBUG_SKIP_TILE", "1")
+    gq.gqa_prefill(dq, dk, dv, dl, 1 / math.sqrt(D), out, lse)
+    assert gq.gqa_decode_check_error() == gq.GQA_ERR_DEVICE_TIMEOUT
+    assert gq.gqa_decode_check_error() == gq.GQA_OK
+
+    monkeypatch.delenv("GQA_DECODE_DEBUG_SKIP_TILE")
+    monkeypatch.delenv("GQA_DECODE_DEBUG_TIMEOUT_MS")
+    ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, 1 / math.sqrt(D), threads=8)
+    for _ in range(2):   # every SM's tensor memory is allocatable again
+        got_out, got_lse = run_gpu(q, k, v, lens, 1 / math.sqrt(D), device_inputs=(dq, dk, dv, dl),
+                                   entry=gq.gqa_prefill)
+        compare(got_out, got_lse, ref_out, ref_lse, what="prefill after timeout")

@@ -9,7 +9,9 @@ head dimensions, lengths shorter than sq (rows that see nothing), empty
 sequences, Tmax not a multiple of the tile, and NaN in every cache entry past
 a sequence's length.
 """
+import contextlib
 import math
+import os
 
 import numpy as np
 import pytest
@@ -27,6 +29,23 @@ def prefill(*args, **kw):
     return run_gpu(*args, entry=gq.gqa_prefill, **kw)
 
 
+@contextlib.contextmanager
+def forced_splits(n):
+    """Key ranges per pair of row tiles (None: the library's plan)."""
+    old = os.environ.get("GQA_PREFILL_SPLITS")
+    if n is None:
+        os.environ.pop("GQA_PREFILL_SPLITS", None)
+    else:
+        os.environ["GQA_PREFILL_SPLITS"] = str(n)
+    try:
+        yield
+    finally:
+        if old is None:
+            os.environ.pop("GQA_PREFILL_SPLITS", None)
+        else:
+            os.environ["GQA_PREFILL_SPLITS"] = old
+
+
 CASES = [  # (B, sq, H, G, D, Tmax, lens)
     (1, 64, 32, 8, 64, 4096, [4096]),          # the page's chunk: 64 new tokens after 4032
     (2, 300, 8, 2, 128, 300, [300, 300]),      # fresh prefill, ragged last row tile
@@ -40,11 +59,16 @@ CASES = [  # (B, sq, H, G, D, Tmax, lens)
 
 @pytest.mark.parametrize("B,sq,H,G,D,Tmax,lens", CASES, ids=lambda x: str(x))
 def test_prefill_vs_oracle(B, sq, H, G, D, Tmax, lens):
+    """Each case in the library's plan, and with every pair's key range split
+    over 3 and over 7 CTAs (partials merged by the combine kernel; ranges that
+    hold no visible key for some rows, and more ranges than key tiles)."""
     q, k, v, lens = make_inputs(B, sq, H, G, D, Tmax, lens, seed=700 + B + sq + H + G + D)
     scale = 1 / math.sqrt(D)
     ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, scale, threads=16)
-    out, lse = prefill(q, k, v, lens, scale)
-    compare(out, lse, ref_out, ref_lse, what=f"prefill B={B} sq={sq} H={H} G={G} D={D}")
+    for n in (None, 3, 7):
+        with forced_splits(n):
+            out, lse = prefill(q, k, v, lens, scale)
+        compare(out, lse, ref_out, ref_lse, what=f"prefill B={B} sq={sq} H={H} G={G} D={D} splits={n}")
 
 
 def test_prefill_equals_decode_definition_small_rows():
