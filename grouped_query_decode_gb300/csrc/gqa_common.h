@@ -95,14 +95,19 @@ struct PrefillParams {
 // fragments in shared memory rather than in registers.
 template <int D, int MT, bool KV8 = false>
 struct KernelShape {
-    static constexpr int kConsumerWarps = kSlices * MT;
+    // fp8 with one row tile: two groups of four consumer warps take
+    // alternate tiles of each segment (a 16 KB fp8 stage is consumed at the
+    // rate of a 32 KB bf16 one otherwise) and merge at the segment's end.
+    static constexpr bool kDual = KV8 && MT == 1;
+    static constexpr int kGroups = kDual ? 2 : 1;
+    static constexpr int kConsumerWarps = kSlices * MT * kGroups;
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;
     // Registers per thread: the 64K register file for one CTA, with warps
     // counted in the allocation steps of 4, in steps of 8 registers, <= 255.
     static constexpr int kAllocWarps = (kThreads / 32 + 3) / 4 * 4;
     static constexpr int kMaxRegs =
         (65536 / (kAllocWarps * 32)) / 8 * 8 > 255 ? 255 : (65536 / (kAllocWarps * 32)) / 8 * 8;
-    static constexpr bool kQInSmem = MT > 1;
+    static constexpr bool kQInSmem = MT > 1 || kDual;
     static constexpr int kQBytesPerWarp = kQInSmem ? 16 * D * 2 : 0;
     // K/V elements as stored in the cache: bf16, or fp8 e4m3 codes (KV8).
     static constexpr int kElemBytes = KV8 ? 1 : 2;
@@ -120,11 +125,14 @@ struct KernelShape {
     static constexpr int kMlBytes = MT * kSlices * 16 * 2 * 4;
     static constexpr int kQBytes = kConsumerWarps * kQBytesPerWarp;
     // fp8 stages are half as large: twice as many keep the same bytes in flight.
-    static constexpr int kStages = KV8 ? (MT == 1 ? 10 : 8) : (D == 128 ? (MT == 1 ? 5 : 4) : 8);
-    static constexpr int kBarBytes = 8 * (2 * kStages + 4 * MT) + 64;
+    static constexpr int kStages = KV8 ? 8 : (D == 128 ? (MT == 1 ? 5 : 4) : 8);
+    // Dual groups: group 1's per-lane state (m, l partials and the O
+    // fragments of each slice) for group 0 to merge.
+    static constexpr int kGroupBytes = kDual ? kSlices * 32 * (D / 8 * 4 + 4) * 4 : 0;
+    static constexpr int kBarBytes = 8 * (2 * kStages + 4 * MT + 2) + 64;
     // +1024 so the ring can be aligned to the 1 KB swizzle atom at run time.
     static constexpr int kSmemBytes =
-        1024 + kStages * kStageBytes + kMergeBytes + kMlBytes + kQBytes + kBarBytes;
+        1024 + kStages * kStageBytes + kMergeBytes + kMlBytes + kQBytes + kGroupBytes + kBarBytes;
 };
 
 }  // namespace gqa

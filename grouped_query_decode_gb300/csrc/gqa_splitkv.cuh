@@ -265,11 +265,13 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     float* merge_buf = reinterpret_cast<float*>(ring_ptr + S * KS::kStageBytes);
     float* ml_buf = merge_buf + KS::kMergeBytes / 4;
     unsigned char* q_smem = reinterpret_cast<unsigned char*>(ml_buf + KS::kMlBytes / 4);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(q_smem + KS::kQBytes);
+    float* group_buf = reinterpret_cast<float*>(q_smem + KS::kQBytes);   // dual groups only
+    uint64_t* bars = reinterpret_cast<uint64_t*>(q_smem + KS::kQBytes + KS::kGroupBytes);
     const uint32_t full_bar = smem_addr(bars);
     const uint32_t empty_bar = full_bar + 8 * S;
     const uint32_t merge_bar = empty_bar + 8 * S;          // [MT][4]: A, B, C, D
-    long long* shared_ll = reinterpret_cast<long long*>(bars + 2 * S + 4 * MT);
+    const uint32_t group_bar = merge_bar + 8 * 4 * MT;     // E, F (dual groups)
+    long long* shared_ll = reinterpret_cast<long long*>(bars + 2 * S + 4 * MT + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(shared_ll + 4);
     volatile int* last_flag = abort_flag + 1;              // [MT]
 
@@ -280,9 +282,12 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar + 8 * s, 1);
-            mbar_init(empty_bar + 8 * s, KS::kConsumerWarps);
+            // Each stage is read by the warps of one group.
+            mbar_init(empty_bar + 8 * s, KS::kConsumerWarps / KS::kGroups);
         }
         for (int m = 0; m < 4 * MT; ++m) mbar_init(merge_bar + 8 * m, kSlices * 32);
+        mbar_init(group_bar, KS::kConsumerWarps * 32);
+        mbar_init(group_bar + 8, KS::kConsumerWarps * 32);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -415,7 +420,8 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
 
     // ---------------------------------------------------------- consumers
     const int slice = warp % kSlices;
-    const int mt = warp / kSlices;
+    const int mt = KS::kDual ? 0 : warp / kSlices;
+    const int group = KS::kDual ? warp / kSlices : 0;     // dual groups: 0 or 1
     const int quad = lane & 3;
     const int grp = lane >> 2;
     const int tid_mt = slice * 32 + lane;                   // 0..127 within the row tile
@@ -440,7 +446,8 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     // matrix m -> tokens 8*(m&1).., 16-byte chunk + (m>>1).
     const int k8_tok = v_tok;
 
-    uint32_t it = 0;
+    uint32_t it_base = 0;      // tiles of this CTA's earlier segments
+    uint32_t e_parity = 0;     // phases of group barriers E and F (dual groups)
     uint32_t seg_parity = 0;   // phases of merge barriers A and B (every segment)
     uint32_t c_parity = 0;     // phases of merge barrier C (partial segments)
     uint32_t d_parity = 0;     // phases of merge barrier D (merges)
@@ -551,17 +558,22 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
         const size_t scale_row = ((size_t)sg.b * p.G + sg.g) * p.scale_tiles;
         float ks_next = 1.f, vs_next = 1.f;
         if constexpr (KV8) {
-            ks_next = __ldg(p.k_scale + scale_row + sg.t0);
-            vs_next = __ldg(p.v_scale + scale_row + sg.t0);
+            if (group < sg.ntiles) {
+                ks_next = __ldg(p.k_scale + scale_row + sg.t0 + group);
+                vs_next = __ldg(p.v_scale + scale_row + sg.t0 + group);
+            }
         }
 
-        for (int i = 0; i < sg.ntiles; ++i, ++it) {
+        // Dual groups take alternate tiles of the segment; otherwise every
+        // consumer warp reads every tile.
+        for (int i = group; i < sg.ntiles; i += KS::kGroups) {
+            const uint32_t it = it_base + i;
             const int s = it % S;
             const float ks = ks_next, vs = vs_next;
             if constexpr (KV8) {
-                if (i + 1 < sg.ntiles) {
-                    ks_next = __ldg(p.k_scale + scale_row + sg.t0 + i + 1);
-                    vs_next = __ldg(p.v_scale + scale_row + sg.t0 + i + 1);
+                if (i + KS::kGroups < sg.ntiles) {
+                    ks_next = __ldg(p.k_scale + scale_row + sg.t0 + i + KS::kGroups);
+                    vs_next = __ldg(p.v_scale + scale_row + sg.t0 + i + KS::kGroups);
                 }
             }
             if (!wait_phase(full_bar + 8 * s, (it / S) & 1, abort_flag, p.status, tmo)) {
@@ -781,7 +793,53 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar + 8 * s);
         }
+        it_base += sg.ntiles;
         if (failed) break;
+
+        if constexpr (KS::kDual) {
+            // ---- group 1 hands each slice's per-lane state (m, partial l,
+            // O fragments) to the same slice and lane of group 0, which
+            // merges it with the log-sum-exp rescale; group 1 then moves on.
+            constexpr int kLaneFloats = NTILE_D * 4 + 4;
+            float* gb = group_buf + (size_t)slice * 32 * kLaneFloats;
+            if (group == 1) {
+                float4* dst = reinterpret_cast<float4*>(gb);
+#pragma unroll
+                for (int n = 0; n < NTILE_D; ++n) dst[n * 32 + lane] = make_float4(o[n][0], o[n][1], o[n][2], o[n][3]);
+                dst[NTILE_D * 32 + lane] = make_float4(m_lo, m_hi, l_lo, l_hi);
+            }
+            mbar_arrive(group_bar);
+            if (!wait_phase(group_bar, e_parity, abort_flag, p.status, tmo)) { failed = true; break; }
+            if (group == 0) {
+                const float4* src = reinterpret_cast<const float4*>(gb);
+                float a_lo, b_lo, a_hi, b_hi;
+                {
+                    const float4 ml = src[NTILE_D * 32 + lane];
+                    const float M_lo = fmaxf(m_lo, ml.x), M_hi = fmaxf(m_hi, ml.y);
+                    a_lo = m_lo == -INFINITY ? 0.f : fast_exp2(m_lo - M_lo);
+                    b_lo = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M_lo);
+                    a_hi = m_hi == -INFINITY ? 0.f : fast_exp2(m_hi - M_hi);
+                    b_hi = ml.y == -INFINITY ? 0.f : fast_exp2(ml.y - M_hi);
+                    l_lo = l_lo * a_lo + ml.z * b_lo;
+                    l_hi = l_hi * a_hi + ml.w * b_hi;
+                    m_lo = M_lo;
+                    m_hi = M_hi;
+                }
+#pragma unroll
+                for (int n = 0; n < NTILE_D; ++n) {
+                    const float4 v = src[n * 32 + lane];
+                    o[n][0] = fmaf(o[n][0], a_lo, v.x * b_lo);
+                    o[n][1] = fmaf(o[n][1], a_lo, v.y * b_lo);
+                    o[n][2] = fmaf(o[n][2], a_hi, v.z * b_hi);
+                    o[n][3] = fmaf(o[n][3], a_hi, v.w * b_hi);
+                }
+            }
+            // The buffer is free again once group 0 has read it.
+            mbar_arrive(group_bar + 8);
+            if (!wait_phase(group_bar + 8, e_parity, abort_flag, p.status, tmo)) { failed = true; break; }
+            e_parity ^= 1;
+            if (group == 1) continue;
+        }
 
         // ---- merge the four slices' (m, l, O) of this row tile
         l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
