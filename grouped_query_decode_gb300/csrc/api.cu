@@ -315,6 +315,9 @@ int gqa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
 int gqa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
                float scale, void* out, float* lse, int B, int sq, int H, int G, int D, int Tmax,
                cudaStream_t stream) {
+    // More than 32 rows per KV head: the same attention on the prefill kernel.
+    if (B > 0 && sq > 0 && H > 0 && G > 0 && H % G == 0 && (long long)(H / G) * sq > 16 * kMaxRowTiles)
+        return gqa_prefill(q, k_cache, v_cache, seq_lens, scale, out, lse, B, sq, H, G, D, Tmax, stream);
     int st = check_shapes(B, sq, H, G, D, Tmax);
     if (st != GQA_OK) return st;
     if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_INVALID_ARG;
@@ -495,7 +498,7 @@ const char* gqa_decode_strerror(int status) {
         case GQA_OK: return "ok";
         case GQA_ERR_INVALID_ARG: return "invalid argument (null pointer or non-positive size)";
         case GQA_ERR_HEAD_RATIO: return "H is not a multiple of G";
-        case GQA_ERR_UNSUPPORTED: return "unsupported shape (D must be 64 or 128, (H/G)*sq <= 32)";
+        case GQA_ERR_UNSUPPORTED: return "unsupported shape (D must be 64 or 128; (H/G)*sq <= 32 except for gqa_decode and gqa_prefill)";
         case GQA_ERR_MISALIGNED: return "a tensor pointer is not 16-byte aligned";
         case GQA_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
         case GQA_ERR_CUDA: return "a CUDA call failed (see gqa_decode_last_cuda_error)";

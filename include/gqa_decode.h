@@ -33,7 +33,11 @@
  *   out      [B, sq, H, D]    bfloat16, round-to-nearest-even of the fp32 result
  *   lse      [B, sq, H]       float32, natural log of sum_t exp(scale * q.k_t)
  *                             over the visible keys; may be NULL (not written)
- * Supported: D in {64, 128}; R = (H/G)*sq <= 32 query rows per KV head.
+ * Supported: D in {64, 128}. gqa_decode accepts any number of query rows per
+ * KV head, R = (H/G)*sq: up to 32 it runs the split-KV decode kernel, above
+ * that the prefill kernel (see gqa_prefill, which also needs scale > 0). The
+ * other decode entry points (workspace, plan, append, paged, fp8, no-alloc)
+ * take R <= 32.
  * A row with no visible key (T_b - sq + s < 0) gets out = 0 and lse = -inf.
  *
  * Ownership and ordering: the caller owns every tensor and the stream. All

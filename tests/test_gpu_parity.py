@@ -191,3 +191,17 @@ def test_every_row_count(H, G, sq):
         with min_tiles(mt):
             out, lse = run_gpu(q, k, v, lens, 0.1)
         compare(out, lse, ref_out, ref_lse, what=f"R={H // G * sq}")
+
+
+@pytest.mark.parametrize("B,sq,H,G,D,lens", [
+    (2, 8, 32, 4, 128, [700, 9]),     # speculative-style: 8 new tokens, group of 8, R = 64
+    (3, 2, 48, 2, 64, [300, 1, 0]),   # R = 48, a sequence shorter than sq, an empty one
+], ids=["R64", "R48"])
+def test_decode_with_more_than_32_rows_per_kv_head(B, sq, H, G, D, lens):
+    """gqa_decode takes any number of rows per KV head; above 32 it runs the
+    prefill kernel on the same definition."""
+    q, k, v, lens = make_inputs(B, sq, H, G, D, 700, lens, seed=210 + H)
+    scale = 1 / math.sqrt(D)
+    ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, scale, threads=8)
+    out, lse = run_gpu(q, k, v, lens, scale)
+    compare(out, lse, ref_out, ref_lse, what=f"decode R={(H // G) * sq}")
