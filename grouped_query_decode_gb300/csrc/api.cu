@@ -426,8 +426,8 @@ int gqa_prefill(const void* q, const void* k_cache, const void* v_cache, const i
     const long long items = (long long)B * G * ((row_tiles + 1) / 2);
     const long long key_tiles = (Tmax + 127) / 128;
     long long splits = 1;
-    if (2 * items < info.sms) {
-        splits = (info.sms + items - 1) / items;
+    if (2 * items <= info.sms) {
+        splits = info.sms / items;   // one wave
         if (splits > key_tiles / 2) splits = key_tiles / 2;
         if (splits < 1) splits = 1;
     }
