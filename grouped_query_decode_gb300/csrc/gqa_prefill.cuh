@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
     const int item = SPLIT ? (int)(blockIdx.x / p.splits) : (int)blockIdx.x;
     const int pr = pairs - 1 - item / units;
     const int unit = item % units;
-    const int b = unit / p.G, g = unit % p.G;
+    const int b = unit / p.G;
     const int tb = clamp_len(__ldg(p.seq_lens + b), p.Tmax);
     const int hpg = p.heads_per_group;
     // Rows and key tiles of tile A (x = 0) and B (x = 1), kept in registers

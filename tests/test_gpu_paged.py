@@ -55,3 +55,26 @@ def test_paged_rejects_bad_page_sizes():
                                   dl.data_ptr(), 0.1, out.data_ptr(), None, 1, 1, 8, 2, 64, ps,
                                   kp.shape[0], table.shape[1], None)
         assert rc == code, ps
+
+
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_out_of_range_page_reads_as_zeros(page_size):
+    """A block-table entry outside [0, num_pages) for a page the sequence uses
+    reads as zeros (no fault): the result is the oracle's over the logical
+    cache with that page's rows zero. 16-token pages go through the producer's
+    lane copies, 64-token pages through TMA boxes."""
+    lens = [200, 130]
+    B, sq, H, G, D, Tmax = 2, 1, 16, 4, 128, 256
+    q, k, v, lens = make_inputs(B, sq, H, G, D, Tmax, lens, seed=720 + page_size)
+    kp, vp, table = syn.paginate(k, v, lens, page_size, seed=721)
+    bad_b, bad_j = 0, 1                      # second page of sequence 0
+    table = table.copy()
+    table[bad_b, bad_j] = kp.shape[0] + 3
+    k0, v0 = k.copy(), v.copy()
+    rows = slice(bad_j * page_size, (bad_j + 1) * page_size)
+    k0[bad_b, :, rows, :] = 0
+    v0[bad_b, :, rows, :] = 0
+    scale = 1 / math.sqrt(D)
+    ref_out, ref_lse = oracle.gqa_decode_f64(q, k0, v0, lens, scale, threads=8)
+    out, lse = _run_paged(q, kp, vp, table, lens, scale)
+    compare(out, lse, ref_out, ref_lse, what=f"bad page ps={page_size}")
