@@ -54,13 +54,18 @@ struct PrefillShape {
     static constexpr int kStages = D == 128 ? 2 : 4;
     static constexpr int kThreads = 11 * 32;
     // k_full, k_empty, v_full, v_empty rings; per tile q_full, s_full,
-    // p_full, o_done, fin.
-    static constexpr int kBars = 4 * kStages + 8 + 4;
+    // p_full, o_done, fin, tok, s_free.
+    static constexpr int kBars = 4 * kStages + 8 + 6;
     static constexpr int kSmemBytes = 1024 + 2 * kQBytes + 2 * kStages * kTileBytes + 8 * kBars + 16;
     static constexpr uint32_t kTmemCols = 512;
     // Columns: S_A | S_B | O_A | O_B.
+    // D = 64 leaves room for P beside S (S_A | S_B | P_A | P_B | O_A | O_B),
+    // so S(j+1) can be computed once the softmax has read S(j); at D = 128
+    // P is written over the first half of S (S_A | S_B | O_A | O_B).
+    static constexpr bool kSepP = D == 64;
     static constexpr uint32_t kColS0 = 0, kColS1 = 128;
-    static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
+    static constexpr uint32_t kColP0 = kSepP ? 256 : kColS0, kColP1 = kSepP ? 320 : kColS1;
+    static constexpr uint32_t kColO0 = kSepP ? 384 : 256, kColO1 = kColO0 + D;
 };
 
 // Lane 0 waits (bounded) and the warp agrees on the outcome.
@@ -94,6 +99,7 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
     const uint32_t o_done = p_full + 16;                     // [2]
     const uint32_t fin = o_done + 16;                        // [2]
     const uint32_t tok = fin + 16;                           // [2] turn tokens of the MMA warps
+    const uint32_t s_free = tok + 16;                        // [2] S read by the softmax (kSepP)
     unsigned char* gen = smem_raw + (bar0 + 8 * PS::kBars - raw);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gen);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gen + 4);
@@ -149,6 +155,8 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
         mbar_init(fin + 8, 1);
         mbar_init(tok, 1);
         mbar_init(tok + 8, 1);
+        mbar_init(s_free, kPfRows);
+        mbar_init(s_free + 8, kPfRows);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -241,16 +249,82 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
             umma_commit(s_full + 8 * x);
             umma_commit(k_empty + 8 * (j % S));    // K_j has had its last reader from this tile
         };
+        const uint32_t p_tm = tmem + (x ? PS::kColP1 : PS::kColP0);
         auto issue_pv = [&](int j) {
             const uint32_t vst = v_s + (j % S) * PS::kTileBytes;
 #pragma unroll
             for (int kk = 0; kk < kPfTokens / 16; ++kk)
-                umma_bf16_ts(o_tm, s_tm + kk * 8, smem_desc_sw128(vst + kk * 16 * 128, kBlock, 1024), kIdescO,
+                umma_bf16_ts(o_tm, p_tm + kk * 8, smem_desc_sw128(vst + kk * 16 * 128, kBlock, 1024), kIdescO,
                              (j > 0 || kk > 0) ? 1u : 0u);
             umma_commit(v_empty + 8 * (j % S));
+            if constexpr (PS::kSepP) umma_commit(o_done + 8 * x);   // one phase per product
+        };
+        auto zero_v_tail = [&](int j) {
+            // Keys past the valid length may hold anything (NaN included);
+            // zero their V rows so that p = 0 times them stays 0. Both MMA
+            // warps may write the same zeros; each does so before its own
+            // product reads them.
+            const int valid = tb - (j0 + j) * kPfTokens;
+            if (valid < kPfTokens) {
+                const uint32_t vst = v_s + (j % S) * PS::kTileBytes;
+                const int first = valid > 0 ? valid : 0;
+                for (int idx = lane; idx < (kPfTokens - first) * PS::kDBlocks * 8; idx += 32) {
+                    const int row = first + idx / (PS::kDBlocks * 8);
+                    const int rest = idx % (PS::kDBlocks * 8);
+                    st_shared_zero16(vst + (rest >> 3) * kBlock + row * 128 + ((rest & 7) << 4));
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
         };
         bool ok = true;
         bool issued_any = false;
+        if constexpr (PS::kSepP) {
+            // S and P apart: S(j+1) as soon as the softmax has read S(j),
+            // P(j) V_j as soon as P(j) is written; the warps need no turns.
+            if (nx > 0) ok = warp_wait(q_full + 8 * x, 0, abort_flag, p.status, tmo) &&
+                             warp_wait(k_full, 0, abort_flag, p.status, tmo);
+            if (ok && nx > 0 && lane == 0) {
+                tc_fence_after();
+                issue_s(0);
+            }
+            issued_any = ok && nx > 0;
+            __syncwarp();
+            for (int j = 0; ok && j < n_all; ++j) {
+                const int sv = j % S;
+                const uint32_t ph = (j / S) & 1;
+                if (j >= nx) {
+                    ok = warp_wait(k_full + 8 * sv, ph, abort_flag, p.status, tmo) &&
+                         warp_wait(v_full + 8 * sv, ph, abort_flag, p.status, tmo);
+                    if (ok && lane == 0) {
+                        mbar_arrive(k_empty + 8 * sv);
+                        mbar_arrive(v_empty + 8 * sv);
+                    }
+                    __syncwarp();
+                    continue;
+                }
+                if (j + 1 < nx) {
+                    ok = warp_wait(s_free + 8 * x, j & 1, abort_flag, p.status, tmo) &&
+                         warp_wait(k_full + 8 * ((j + 1) % S), ((j + 1) / S) & 1, abort_flag, p.status, tmo);
+                    if (!ok) break;
+                    if (lane == 0) {
+                        tc_fence_after();
+                        issue_s(j + 1);
+                    }
+                    __syncwarp();
+                }
+                ok = warp_wait(v_full + 8 * sv, ph, abort_flag, p.status, tmo);
+                if (!ok) break;
+                zero_v_tail(j);
+                ok = warp_wait(p_full + 8 * x, j & 1, abort_flag, p.status, tmo);
+                if (!ok) break;
+                if (lane == 0) {
+                    tc_fence_after();
+                    issue_pv(j);
+                }
+                __syncwarp();
+            }
+        } else {
         // The two warps take turns: A issues S_A(0), then B S_B(0), then A
         // its batch {P_A(0) V_0, S_A(1)}, then B its batch, and so on; turn
         // k of warp x is arrival k on tok[x], which the other warp waits for
@@ -294,22 +368,7 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
             }
             ok = warp_wait(v_full + 8 * sv, ph, abort_flag, p.status, tmo);
             if (!ok) break;
-            // Keys past the valid length may hold anything (NaN included);
-            // zero their V rows so that p = 0 times them stays 0. Both MMA
-            // warps may write the same zeros; each does so before its own
-            // product reads them.
-            const int valid = tb - (j0 + j) * kPfTokens;
-            if (valid < kPfTokens) {
-                const uint32_t vst = v_s + sv * PS::kTileBytes;
-                const int first = valid > 0 ? valid : 0;
-                for (int idx = lane; idx < (kPfTokens - first) * PS::kDBlocks * 8; idx += 32) {
-                    const int row = first + idx / (PS::kDBlocks * 8);
-                    const int rest = idx % (PS::kDBlocks * 8);
-                    st_shared_zero16(vst + (rest >> 3) * kBlock + row * 128 + ((rest & 7) << 4));
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
+            zero_v_tail(j);
             ok = warp_wait(p_full + 8 * x, j & 1, abort_flag, p.status, tmo);
             if (ok && j + 1 < nx)
                 ok = warp_wait(k_full + 8 * ((j + 1) % S), ((j + 1) / S) & 1, abort_flag, p.status, tmo);
@@ -325,6 +384,7 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
             }
             end_turn();
         }
+        }   // kSepP
         // Every MMA this warp issued has completed once `fin` flips.
         if (issued_any && lane == 0) {
             umma_commit(fin + 8 * x);
@@ -395,6 +455,11 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < kPfTokens; ++i) xs[i] = __uint_as_float(u[i]);
             }
+            if constexpr (PS::kSepP) {
+                // S(j) is in registers: its columns may take S(j+1).
+                tc_fence_before();
+                mbar_arrive(s_free + 8 * x);
+            }
             // Invisible keys -> -inf (only tiles that reach past this row's
             // limit). The max is taken on the raw scores (scale > 0) with eight
             // independent partial maxima and sums, so that no dependency chain
@@ -430,8 +495,20 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
                 pk[i / 2] = pack_bf16x2(e0, e1);
             }
             const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+            if constexpr (PS::kSepP) {
+                // P_X(j-1) V_{j-1} has completed: P's columns are free and O
+                // is settled (with S apart, S(j) no longer implies it).
+                if (j > 0) {
+                    ok = wait_phase(o_done + 8 * x, (j - 1) & 1, abort_flag, p.status, tmo);
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+            }
             if (j > 0 && __any_sync(0xffffffffu, up)) {
-                // O_X holds P_X(j-1) V_{j-1} already (see above): rescale it.
+                // O_X holds P_X(j-1) V_{j-1} already: rescale it.
                 const float alpha = up ? fast_exp2(m - base_m) : 1.f;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -445,14 +522,14 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
             if (up) l *= fast_exp2(m - base_m);
             m = mn;
             l += sum;
-            // P (bf16 pairs) over the first 64 columns of S_X.
-            tmem_st64(lane_addr + col_s, pk);
+            // P (bf16 pairs): its own columns at D = 64, the first 64 of S_X at D = 128.
+            tmem_st64(lane_addr + (x ? PS::kColP1 : PS::kColP0), pk);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(p_full + 8 * x);
         }
         if (ok && n > 0) {
-            ok = wait_phase(o_done + 8 * x, 0, abort_flag, p.status, tmo);
+            ok = wait_phase(o_done + 8 * x, PS::kSepP ? (n - 1) & 1 : 0, abort_flag, p.status, tmo);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) tc_fence_after();
         }
