@@ -15,6 +15,9 @@ constexpr float kRescaleSlack = 8.0f;   // lazy online-softmax rescale threshold
 // Most CTAs whose partials one merge can combine (the merge keeps per-
 // contributor state in shared memory); the grid never exceeds it.
 constexpr int kMaxMergeContrib = 180;
+// Units split over at most this many CTAs are merged by each thread in one
+// round of loads; more contributors take the cooperative three-step merge.
+constexpr int kFastMerge = 8;
 
 // Status bits of the per-device status word.
 constexpr unsigned kStatusTimeout = 1u;

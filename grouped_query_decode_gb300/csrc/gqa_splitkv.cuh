@@ -990,12 +990,16 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             __threadfence();
             __syncwarp();
             if (lane == 0) {
-                unsigned contributors = 0;
-                for (long long c = cf; c <= cl; ++c)
-                    contributors += (c * W / P) < ((c + 1) * W / P) ? 1u : 0u;
+                // With at least one tile per CTA every CTA from cf to cl has
+                // a share of the unit; otherwise count the non-empty ones.
+                unsigned contributors = (unsigned)(cl - cf + 1);
+                if (W < P) {
+                    contributors = 0;
+                    for (long long c = cf; c <= cl; ++c)
+                        contributors += (c * W / P) < ((c + 1) * W / P) ? 1u : 0u;
+                }
                 const unsigned arrived = arrive_unit(
                     p.ws_counters + ((size_t)sg.b * p.G + sg.g) * kMaxRowTiles + mt, p.epoch, p.status);
-                __threadfence();  // the other contributors' partials are visible from here on
                 last_flag[mt] = arrived == contributors ? 1 : 0;
             }
         }
@@ -1003,7 +1007,60 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
         if (!wait_phase(mbarC, c_parity, abort_flag, p.status, tmo)) { failed = true; break; }
         c_parity ^= 1;
         if (!last_flag[mt]) continue;
-        __threadfence();
+        __threadfence();   // the other contributors' partials are visible from here on
+
+        if (W >= P && cl - cf < kFastMerge) {
+            // ---- few contributors (every CTA from cf to cl has a share): each
+            // thread merges four columns of one row in a single round of
+            // independent loads. Slot 0 is a CTA's first segment: for every
+            // CTA after cf this unit is where its share starts; cf's share
+            // starts at the unit's first tile exactly when cf * W / P == ub.
+            const int ncand = (int)(cl - cf + 1);
+            const int first_slot = (int)(cf * 2 + ((cf * W / P) == sg.ub ? 0 : 1));
+            const int rows_here = (p.R - mt * 16) < 16 ? (p.R - mt * 16) : 16;
+            constexpr int C4 = D / 4;
+            for (int item = tid_mt; item < rows_here * C4; item += kSlices * 32) {
+                const int rr = item / C4;
+                const int r = mt * 16 + rr;
+                const int c4 = (item % C4) * 4;
+                float mk[kFastMerge], lk[kFastMerge];
+                float4 ok4[kFastMerge];
+#pragma unroll
+                for (int k = 0; k < kFastMerge; ++k) {
+                    mk[k] = -INFINITY;
+                    lk[k] = 0.f;
+                    ok4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (k < ncand) {
+                        const int sl = k == 0 ? first_slot : (int)((cf + k) * 2);
+                        const float* base = p.ws_part + (size_t)sl * slot_floats;
+                        mk[k] = __ldcg(base + (size_t)p.R * D + r);
+                        lk[k] = __ldcg(base + (size_t)p.R * D + p.R + r);
+                        ok4[k] = __ldcg(reinterpret_cast<const float4*>(base + (size_t)r * D + c4));
+                    }
+                }
+                float M = mk[0];
+#pragma unroll
+                for (int k = 1; k < kFastMerge; ++k) M = fmaxf(M, mk[k]);
+                float L = 0.f;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < kFastMerge; ++k) {
+                    const float w = (mk[k] == -INFINITY || lk[k] == 0.f) ? 0.f : lk[k] * fast_exp2(mk[k] - M);
+                    L += w;
+                    acc.x += w * ok4[k].x;
+                    acc.y += w * ok4[k].y;
+                    acc.z += w * ok4[k].z;
+                    acc.w += w * ok4[k].w;
+                }
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                const int j = r / p.sq, s = r % p.sq;
+                const int row = (sg.b * p.sq + s) * p.H + sg.g * p.heads_per_group + j;
+                *reinterpret_cast<uint2*>(p.out + (size_t)row * D + c4) =
+                    make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+                if (c4 == 0 && p.lse) p.lse[row] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+            }
+            continue;
+        }
 
         // ---- this CTA arrived last: merge the unit's partials for the rows
         // of this row tile with the log-sum-exp rescale
