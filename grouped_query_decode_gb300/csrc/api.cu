@@ -78,11 +78,28 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // A cache of `slabs` slabs of [rows][D] bf16 -- [B*G units][Tmax][D] for a
 // contiguous cache, [pages*G][page_size][D] for a paged one -- viewed as a 3-D
 // tensor; boxes of box_rows rows x 64 elements (128 bytes) with the 128-byte
-// swizzle. Reads past a slab's rows, or of a slab out of range, give 0.
+// swizzle (with both_halves, a bf16 D = 128 cache is viewed as 4-D instead and
+// a box covers both 64-column halves). Reads past a slab's rows, or of a slab
+// out of range, give 0.
 int encode_cache_map(CUtensorMap* map, const void* base, long long slabs, int rows, int D,
-                     int box_rows, int elem_bytes = 2) {
+                     int box_rows, int elem_bytes = 2, bool both_halves = false) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return cuda_fail(cudaErrorNotSupported);
+    if (both_halves && elem_bytes == 2 && D == 128) {
+        // bf16 rows of 256 bytes as [64 columns][rows][2 halves][slabs]: the
+        // halves' stride (128 B) is below the rows' (256 B), so one box of
+        // box_rows rows x both halves lands as [half][row][128 B] -- the two
+        // 64-column blocks of the stage -- in one copy.
+        cuuint64_t dims[4] = {64, (cuuint64_t)rows, 2, (cuuint64_t)slabs};
+        cuuint64_t strides[3] = {(cuuint64_t)D * 2, 128, (cuuint64_t)rows * D * 2};
+        cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 2, 1};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+        return GQA_OK;
+    }
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)slabs};
     cuuint64_t strides[2] = {(cuuint64_t)D * elem_bytes, (cuuint64_t)rows * D * elem_bytes};
     cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes), (cuuint32_t)box_rows, 1};
@@ -233,9 +250,13 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32
     const long long slabs = pg.block_table ? (long long)pg.num_pages * G : (long long)B * G;
     const int rows = pg.block_table ? pg.page_size : Tmax;
     const int box_rows = pg.block_table && pg.page_size < kTileTokens ? pg.page_size : kTileTokens;
-    st = encode_cache_map(&a.tm_k, k_cache, slabs, rows, D, box_rows, kv8 ? 1 : 2);
+    // Pages shorter than a tile, one row tile: the kernel's stage is
+    // page-major and one box per page brings both halves of a bf16 D = 128
+    // row (the 4-D view); elsewhere one 3-D box per half (measured as fast).
+    const bool both_halves = box_rows < kTileTokens && plan.row_tiles == 1;
+    st = encode_cache_map(&a.tm_k, k_cache, slabs, rows, D, box_rows, kv8 ? 1 : 2, both_halves);
     if (st != GQA_OK) return st;
-    st = encode_cache_map(&a.tm_v, v_cache, slabs, rows, D, box_rows, kv8 ? 1 : 2);
+    st = encode_cache_map(&a.tm_v, v_cache, slabs, rows, D, box_rows, kv8 ? 1 : 2, both_halves);
     if (st != GQA_OK) return st;
     a.p.q = static_cast<const uint16_t*>(q);
     a.p.seq_lens = seq_lens;

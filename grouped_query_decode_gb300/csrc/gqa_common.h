@@ -111,6 +111,11 @@ struct KernelShape {
     static constexpr int kMaxRegs =
         (65536 / (kAllocWarps * 32)) / 8 * 8 > 255 ? 255 : (65536 / (kAllocWarps * 32)) / 8 * 8;
     static constexpr bool kQInSmem = MT > 1 || kDual;
+    // bf16 at D = 128 with one row tile: with pages shorter than a tile the
+    // stage is page-major (one 4-D box per page brings both 64-column blocks
+    // of its rows). Two row tiles keep the block-major stage, whose block
+    // offset is a constant (a runtime one cost them 3%), and one box per block.
+    static constexpr bool kPageMajor = !KV8 && D == 128 && MT == 1;
     static constexpr int kQBytesPerWarp = kQInSmem ? 16 * D * 2 : 0;
     // K/V elements as stored in the cache: bf16, or fp8 e4m3 codes (KV8).
     static constexpr int kElemBytes = KV8 ? 1 : 2;

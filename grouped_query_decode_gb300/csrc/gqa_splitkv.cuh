@@ -104,6 +104,26 @@ __device__ __forceinline__ long long cta_of_tile(long long x, long long W, long 
     return ((x + 1) * P - 1) / W;
 }
 
+// Byte offset of row r (0..63), 64-column block bx, in a stage of a cache
+// with P = 2^lp rows per TMA box (P = 64, one box per tile, or the page size
+// of a paged cache with shorter pages): boxes of P rows are laid out one
+// after the other, each as [block][row][128 B], with the 128-byte swizzle
+// applied by the caller on the 16-byte chunk. At lp = 6 this is
+// [block][64 rows][128 B].
+template <int NB>
+__device__ __forceinline__ uint32_t stage_off(int r, int bx, int lp) {
+    return (uint32_t)((((r >> lp) * NB + bx) << (lp + 7)) + ((r & ((1 << lp) - 1)) << 7));
+}
+
+// The same for a kernel shape: page-major stages (KernelShape::kPageMajor)
+// take lp at run time; the others are always [block][64 rows][128 B], with
+// the block offset a constant.
+template <class KS>
+__device__ __forceinline__ uint32_t stage_row_off(int r, int bx, int lp) {
+    if constexpr (KS::kPageMajor) return stage_off<KS::kBoxes>(r, bx, lp);
+    else return (uint32_t)(bx * (kTileTokens * 128) + r * 128);
+}
+
 // One tile of the CTA's share, with where its rows live. For a paged cache a
 // 64-token tile covers part of one page (pages of >= 64 tokens) or
 // 64 / page_size whole pages; `page` holds their physical numbers (pages that
@@ -118,7 +138,7 @@ struct TileRef {
 // consumers are done with the tile S places earlier. The next tile is looked
 // up one step ahead, so that its block-table reads (paged caches) are in
 // flight while the producer waits for a free stage.
-template <int D, int S, bool KV8>
+template <int D, int MT, int S, bool KV8>
 struct TileIssuer {
     SegmentWalker walk;
     Segment sg;
@@ -183,7 +203,7 @@ struct TileIssuer {
                                  const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                  const DecodeParams& p, uint32_t it) {
         if (blockIdx.x == 0 && (int)it == p.skip_tile) return;  // injected fault
-        using KS = KernelShape<D, 1, KV8>;
+        using KS = KernelShape<D, MT, KV8>;
         constexpr int kStageBytes = KS::kStageBytes;
         constexpr int kTileBytes = KS::kTileBytes;
         constexpr int NB = KS::kBoxes;
@@ -211,7 +231,8 @@ struct TileIssuer {
             }
         } else {
             // One box of page_size rows per page that starts before the end of
-            // the sequence; rows past the length are never used (masked, and
+            // the sequence, at that page's place in the stage (stage_off with
+            // P = page_size); rows past the length are never used (masked, and
             // zeroed in V), so the pages after the last one are not read.
             const int ps = p.page_size;
             int npages = 0;
@@ -222,11 +243,21 @@ struct TileIssuer {
             for (int j = 0; j < 4; ++j) {
                 if (r.page[j] < 0) continue;
                 const int z = r.page[j] * p.G + r.g;
+                // Page j's rows at stage_off(j * ps, 0, lp).
+                const uint32_t off = (uint32_t)(j * (KS::kPageMajor ? NB : 1) * ps * 128);
+                // Page-major stage (KernelShape::kPageMajor): the tensor map is
+                // 4-D and one box brings both 64-column blocks of the page's
+                // rows (per-box overhead, not bytes, bounds these short
+                // copies); else one box per block.
+                if constexpr (KS::kPageMajor) {
+                    tma_load_4d(kdst + off, tm_k, fb, 0, 0, 0, z);
+                    tma_load_4d(vdst + off, tm_v, fb, 0, 0, 0, z);
+                } else {
 #pragma unroll
-                for (int bx = 0; bx < NB; ++bx) {
-                    const uint32_t off = bx * (kTileTokens * 128) + j * ps * 128;
-                    tma_load_3d(kdst + off, tm_k, fb, bx * kBoxCols, 0, z);
-                    tma_load_3d(vdst + off, tm_v, fb, bx * kBoxCols, 0, z);
+                    for (int bx = 0; bx < NB; ++bx) {
+                        tma_load_3d(kdst + off + bx * (kTileTokens * 128), tm_k, fb, bx * kBoxCols, 0, z);
+                        tma_load_3d(vdst + off + bx * (kTileTokens * 128), tm_v, fb, bx * kBoxCols, 0, z);
+                    }
                 }
             }
         }
@@ -406,7 +437,7 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     if (is_producer) {
         // ------------------------------------------ dedicated producer warp
         if (lane != 0) return;
-        TileIssuer<D, S, KV8> issuer;
+        TileIssuer<D, MT, S, KV8> issuer;
         issuer.walk = walk;
         issuer.start(p);
         bool done = false;
@@ -445,6 +476,13 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     // e4m3 K and V (one byte per element, one 128-byte box row per token):
     // matrix m -> tokens 8*(m&1).., 16-byte chunk + (m>>1).
     const int k8_tok = v_tok;
+    // Stage layout (stage_row_off): boxes of 2^lp rows -- the page size for a
+    // paged cache with pages shorter than a tile, else the whole tile.
+    const int lp = (KS::kPageMajor && p.block_table != nullptr && p.page_size < kTileTokens)
+                       ? 31 - __clz(p.page_size) : 6;
+    // Block 1 of a row sits 2^(lp+7) bytes after block 0 (stage_off).
+    const uint32_t k_off0 = stage_row_off<KS>(k_tok, 0, lp), v_off0 = stage_row_off<KS>(v_tok, 0, lp);
+    const uint32_t bx_stride = KS::kPageMajor ? 1u << (lp + 7) : kTileTokens * 128;
 
     uint32_t it_base = 0;      // tiles of this CTA's earlier segments
     uint32_t e_parity = 0;     // phases of group barriers E and F (dual groups)
@@ -594,8 +632,7 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                     const int chunk = idx % kChunks;
                     if (tbase + row >= sg.tb) {
                         const int bx = chunk >> 3, cc = chunk & 7;
-                        st_shared_zero16(vst + bx * (kTileTokens * 128) + row * 128 +
-                                         ((cc ^ (row & 7)) << 4));
+                        st_shared_zero16(vst + stage_row_off<KS>(row, bx, lp) + ((cc ^ (row & 7)) << 4));
                         wrote = true;
                     }
                 }
@@ -621,8 +658,7 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                         const uint4 kv = __ldg(reinterpret_cast<const uint4*>(p.k_new + src));
                         const uint4 vv = __ldg(reinterpret_cast<const uint4*>(p.v_new + src));
                         const int row = t - tbase;
-                        const uint32_t off = (chunk >> 3) * (kTileTokens * 128) + row * 128 +
-                                             (((chunk & 7) ^ (row & 7)) << 4);
+                        const uint32_t off = stage_row_off<KS>(row, chunk >> 3, lp) + (((chunk & 7) ^ (row & 7)) << 4);
                         st_shared_v4(kst + off, kv);
                         st_shared_v4(vst + off, vv);
                         if (mt == 0) {
@@ -668,7 +704,11 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                     const int chunk = kk * 2 + k_half;
                     const int bx = chunk >> 3, cc = chunk & 7;
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kst + bx * (kTileTokens * 128) + k_tok * 128 + ((cc ^ (k_tok & 7)) << 4), b0, b1, b2, b3);
+                    if constexpr (KS::kPageMajor)
+                        ldsm_x4(kst + k_off0 + bx * bx_stride + ((cc ^ (k_tok & 7)) << 4), b0, b1, b2, b3);
+                    else
+                        ldsm_x4(kst + bx * (kTileTokens * 128) + k_tok * 128 + ((cc ^ (k_tok & 7)) << 4), b0, b1,
+                                b2, b3);
                     uint32_t a_s[4];
                     if constexpr (kQs) {
                         const int qc = kk * 2 + (lane >> 4);
@@ -784,8 +824,11 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                     const int chunk = n + v_dt;
                     const int bx = chunk >> 3, cc = chunk & 7;
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4_trans(vst + bx * (kTileTokens * 128) + v_tok * 128 + ((cc ^ (v_tok & 7)) << 4), b0, b1,
-                                  b2, b3);
+                    if constexpr (KS::kPageMajor)
+                        ldsm_x4_trans(vst + v_off0 + bx * bx_stride + ((cc ^ (v_tok & 7)) << 4), b0, b1, b2, b3);
+                    else
+                        ldsm_x4_trans(vst + bx * (kTileTokens * 128) + v_tok * 128 + ((cc ^ (v_tok & 7)) << 4), b0,
+                                      b1, b2, b3);
                     mma_bf16_16816(o[n], pa, b0, b1);
                     mma_bf16_16816(o[n + 1], pa, b2, b3);
                 }

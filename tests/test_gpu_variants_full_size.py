@@ -49,9 +49,11 @@ def test_fp8_full_size_sampled_units(name):
         compare(out[b:b + 1, :, heads], lse[b:b + 1, :, heads], ref_o, ref_l, what=f"{name} fp8 b={b} g={g}")
 
 
-@pytest.mark.parametrize("page_size", [16, 256])
-def test_paged_full_size_equals_contiguous(page_size):
-    cfg = syn.config_by_name("llama3_8b_layer")
+@pytest.mark.parametrize("name,page_size", [("llama3_8b_layer", 16), ("llama3_8b_layer", 256), ("mqa_end", 16)])
+def test_paged_full_size_equals_contiguous(name, page_size):
+    """One row tile (page-major stage at 16-token pages) and two row tiles
+    (MQA end: block-major stage)."""
+    cfg = syn.config_by_name(name)
     q, k, v, lens = syn.make_inputs(cfg, threads=16)
     kp, vp, table = syn.paginate(k, v, lens, page_size, seed=cfg.seed + 100)
     cont_out, cont_lse = run_gpu(q, k, v, lens, cfg.scale)
