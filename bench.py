@@ -45,7 +45,7 @@ DEFAULT_WORKLOAD = "llama3_8b_layer"
 PROFILES = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = [os.path.join(ROOT, "grouped_query_decode_gb300", "csrc", f) for f in
                   ("gqa_splitkv.cuh", "gqa_device.cuh", "gqa_common.h", "ptx.cuh", "gqa_launch_impl.cuh",
-                   "api.cu")]
+                   "gqa_decode_tc.cuh", "tcgen05.cuh", "api.cu")]
 
 
 # ------------------------------------------------------------ accounting

@@ -163,6 +163,16 @@ void debug_knobs(unsigned long long* timeout_ns, int* skip_tile) {
     *skip_tile = k ? std::atoi(k) : -1;
 }
 
+// GQA_DECODE_TC=1 runs 17..32-row bf16 decode on the tcgen05 kernel instead
+// of the m16n8k16 split-KV kernel. It is opt-in: measured on the MQA end
+// (95 against 60 us) and the ragged sq = 4 workload (847 against 694 us), its
+// per-tile rate is higher but each segment boundary, first tile and merge
+// waits on global round trips behind the copy stream.
+bool tc_decode_enabled() {
+    const char* s = std::getenv("GQA_DECODE_TC");
+    return s && s[0] == '1';
+}
+
 // Grid size override for sweeps of the plan (unset: the heuristic decides).
 int forced_ctas() {
     const char* s = std::getenv("GQA_DECODE_CTAS");
@@ -247,9 +257,14 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32
         return GQA_ERR_WORKSPACE;
 
     LaunchArgs a;
+    // Two row tiles (17..32 rows), bf16, D = 128, contiguous cache, no fused
+    // append: the tcgen05 kernel, on 128-token tiles.
+    const bool tc = tc_decode_enabled() && !kv8 && D == 128 && plan.row_tiles == 2 && !pg.block_table &&
+                    !k_new;
     const long long slabs = pg.block_table ? (long long)pg.num_pages * G : (long long)B * G;
     const int rows = pg.block_table ? pg.page_size : Tmax;
-    const int box_rows = pg.block_table && pg.page_size < kTileTokens ? pg.page_size : kTileTokens;
+    const int box_rows =
+        tc ? kTcTokens : (pg.block_table && pg.page_size < kTileTokens ? pg.page_size : kTileTokens);
     // Pages shorter than a tile, one row tile: the kernel's stage is
     // page-major and one box per page brings both halves of a bf16 D = 128
     // row (the 4-D view); elsewhere one 3-D box per half (measured as fast).
@@ -291,7 +306,7 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32
     a.row_tiles = plan.row_tiles;
     a.pdl = true;
     a.stream = stream;
-    cudaError_t e = kv8 ? launch_d128_fp8(a) : (D == 64 ? launch_d64(a) : launch_d128(a));
+    cudaError_t e = tc ? launch_decode_tc(a) : kv8 ? launch_d128_fp8(a) : (D == 64 ? launch_d64(a) : launch_d128(a));
     if (e != cudaSuccess) return cuda_fail(e);
     return GQA_OK;
 }

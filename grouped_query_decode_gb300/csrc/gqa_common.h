@@ -19,6 +19,11 @@ constexpr int kMaxMergeContrib = 180;
 // round of loads; more contributors take the cooperative three-step merge.
 constexpr int kFastMerge = 8;
 
+// The tensor-core decode kernel (17..32 rows per KV head, bf16, D = 128):
+// tokens per K/V tile (its MMAs' M) and the rows it serves (their N).
+constexpr int kTcTokens = 128;
+constexpr int kTcRows = 32;
+
 // Status bits of the per-device status word.
 constexpr unsigned kStatusTimeout = 1u;
 

@@ -28,4 +28,12 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     }
 }
 
+// Lane 0 waits (bounded) and the warp agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned* status, uint64_t timeout_ns) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = wait_phase(bar, parity, abort_flag, status, timeout_ns);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 }  // namespace gqa

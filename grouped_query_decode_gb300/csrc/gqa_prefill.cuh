@@ -68,14 +68,6 @@ struct PrefillShape {
     static constexpr uint32_t kColO0 = kSepP ? 384 : 256, kColO1 = kColO0 + D;
 };
 
-// Lane 0 waits (bounded) and the warp agrees on the outcome.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned* status, uint64_t timeout_ns) {
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = wait_phase(bar, parity, abort_flag, status, timeout_ns);
-    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-}
-
 template <int D, bool SPLIT>
 __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
     gqa_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,

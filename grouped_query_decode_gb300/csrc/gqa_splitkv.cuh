@@ -40,11 +40,15 @@ struct Segment {
     bool first;          // the CTA's first segment (partial slot 0, else slot 1)
 };
 
-__device__ __forceinline__ long long tiles_of(int tb) { return (tb + kTileTokens - 1) / kTileTokens; }
+// Tiles of TT tokens covering tb valid tokens.
+template <int TT = kTileTokens>
+__device__ __forceinline__ long long tiles_of(int tb) { return (tb + TT - 1) / TT; }
 
-// Walks the CTA's share [lo, hi) of the flattened tile list, one segment at a
-// time. Every warp runs its own copy; they all see the same sequence.
-struct SegmentWalker {
+// Walks the CTA's share [lo, hi) of the flattened list of TT-token tiles, one
+// segment at a time. Every warp runs its own copy; they all see the same
+// sequence.
+template <int TT = kTileTokens>
+struct SegmentWalkerT {
     const int32_t* seq_lens;
     int G, Tmax;
     long long x, lo, hi, pre_b;
@@ -53,7 +57,7 @@ struct SegmentWalker {
     __device__ bool next(Segment& s) {
         while (x < hi) {
             const int tb = clamp_len(__ldg(seq_lens + b), Tmax);
-            const long long nt = tiles_of(tb);
+            const long long nt = tiles_of<TT>(tb);
             const long long span = nt * G;
             if (x >= pre_b + span) {
                 pre_b += span;
@@ -79,6 +83,7 @@ struct SegmentWalker {
         return false;
     }
 };
+using SegmentWalker = SegmentWalkerT<>;
 
 // Counts one arrival on a unit's counter and returns the arrivals so far in
 // this call. The counter holds (epoch << 16) | count; the first arrival of a
@@ -279,6 +284,100 @@ struct TileIssuer {
     }
 };
 
+// One warp: total tiles W (of TT tokens), the number of CTAs that share
+// them, and where this CTA's share starts, into shared_ll[0..3] = W, first
+// sequence, tiles before it, P. Lengths are read once; lane i keeps
+// sequences i, i+32, ... of the first 256.
+//
+// When every unit has the same number of tiles (all lengths equal), the
+// tiles are shared by fewer CTAs if a grid that keeps at least 80% of
+// them busy lines up with the units: a whole number of units per CTA (no
+// unit split, nothing to merge), or, with fewer units than CTAs, the same
+// whole number of CTAs per unit (every CTA one equal partial) on about 85%
+// of the grid (kSplitEven; a kernel whose merges are cheap keeps every CTA).
+// The CTAs left over exit.
+template <int TT, bool kSplitEven = true>
+__device__ __forceinline__ void plan_share(const DecodeParams& p, int lane, long long* shared_ll) {
+    constexpr int kCached = 8;       // sequences 0..255 stay in registers
+    long long cached[kCached];
+    long long total = 0;
+    int nt_min = 0x7fffffff, nt_max = 0;
+    auto tiles_times_g = [&](int b) -> long long {
+        if (b >= p.B) return 0;
+        const int nt = (int)tiles_of<TT>(clamp_len(__ldg(p.seq_lens + b), p.Tmax));
+        nt_min = min(nt_min, nt);
+        nt_max = max(nt_max, nt);
+        return (long long)nt * p.G;
+    };
+    auto scan_add = [&](long long v) {
+        long long incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        return incl;
+    };
+#pragma unroll
+    for (int k = 0; k < kCached; ++k) {
+        cached[k] = 0;
+        if (k * 32 < p.B) {
+            cached[k] = tiles_times_g(k * 32 + lane);
+            long long sum = cached[k];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            total += sum;
+        }
+    }
+    for (int b0 = kCached * 32; b0 < p.B; b0 += 32)
+        total += __shfl_sync(0xffffffffu, scan_add(tiles_times_g(b0 + lane)), 31);
+    nt_min = __reduce_min_sync(0xffffffffu, nt_min);
+    nt_max = __reduce_max_sync(0xffffffffu, nt_max);
+    long long P = p.ctas;
+    if (p.even_rule && nt_min == nt_max && nt_max > 0) {
+        const long long units = (long long)p.B * p.G;
+        if (units >= P) {
+            const long long per = (units + P - 1) / P;
+            const long long even = (units + per - 1) / per;
+            if (units % per == 0 && 5 * even >= 4 * P) P = even;
+        } else if (kSplitEven) {
+            // Measured on the long-context and MQA-end workloads: about
+            // 85% of the SMs, each unit split evenly, beats every SM with
+            // uneven splits (fewer partials, HBM still saturated).
+            const long long even = units * ((P * 85 / 100) / units);
+            if (even >= units && 5 * even >= 4 * P) P = even;
+        }
+    }
+    // First sequence whose tiles reach past lo, and the tiles before it.
+    const long long lo = (long long)blockIdx.x * total / P;
+    long long pre = 0;
+    int bstart = p.B;
+    long long prestart = total;
+    bool found = (long long)blockIdx.x >= P;
+    auto find = [&](int b0, long long v) {
+        const long long incl = scan_add(v);
+        const unsigned hit = __ballot_sync(0xffffffffu, b0 + lane < p.B && pre + incl > lo);
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            bstart = b0 + src;
+            prestart = pre + __shfl_sync(0xffffffffu, incl - v, src);
+            found = true;
+        } else {
+            pre += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    };
+#pragma unroll
+    for (int k = 0; k < kCached; ++k)
+        if (!found && k * 32 < p.B) find(k * 32, cached[k]);
+    for (int b0 = kCached * 32; !found && b0 < p.B; b0 += 32) find(b0, tiles_times_g(b0 + lane));
+    if (lane == 0) {
+        shared_ll[0] = total;
+        shared_ll[1] = bstart;
+        shared_ll[2] = prestart;
+        shared_ll[3] = P;
+    }
+}
+
 template <int D, int MT, bool KV8>
 __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     gqa_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -329,96 +428,8 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     // Inputs may be written by the previous grid in the stream.
     pdl_wait_primary();
 
-    // Warp 0: total tiles W, the number of CTAs that share them, and where
-    // this CTA's share starts. Lengths are read once; lane i keeps sequences
-    // i, i+32, ... of the first 256.
-    //
-    // When every unit has the same number of tiles (all lengths equal), the
-    // tiles are shared by fewer CTAs if a grid that keeps at least 80% of
-    // them busy lines up with the units: a whole number of units per CTA (no
-    // unit split, nothing to merge), or, with fewer units than CTAs, the same
-    // whole number of CTAs per unit (every CTA one equal partial) on about 85%
-    // of the grid. The CTAs left over exit.
-    if (warp == 0) {
-        constexpr int kCached = 8;       // sequences 0..255 stay in registers
-        long long cached[kCached];
-        long long total = 0;
-        int nt_min = 0x7fffffff, nt_max = 0;
-        auto tiles_times_g = [&](int b) -> long long {
-            if (b >= p.B) return 0;
-            const int nt = (int)tiles_of(clamp_len(__ldg(p.seq_lens + b), p.Tmax));
-            nt_min = min(nt_min, nt);
-            nt_max = max(nt_max, nt);
-            return (long long)nt * p.G;
-        };
-        auto scan_add = [&](long long v) {
-            long long incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const long long n = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += n;
-            }
-            return incl;
-        };
-#pragma unroll
-        for (int k = 0; k < kCached; ++k) {
-            cached[k] = 0;
-            if (k * 32 < p.B) {
-                cached[k] = tiles_times_g(k * 32 + lane);
-                long long sum = cached[k];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-                total += sum;
-            }
-        }
-        for (int b0 = kCached * 32; b0 < p.B; b0 += 32)
-            total += __shfl_sync(0xffffffffu, scan_add(tiles_times_g(b0 + lane)), 31);
-        nt_min = __reduce_min_sync(0xffffffffu, nt_min);
-        nt_max = __reduce_max_sync(0xffffffffu, nt_max);
-        long long P = p.ctas;
-        if (p.even_rule && nt_min == nt_max && nt_max > 0) {
-            const long long units = (long long)p.B * p.G;
-            if (units >= P) {
-                const long long per = (units + P - 1) / P;
-                const long long even = (units + per - 1) / per;
-                if (units % per == 0 && 5 * even >= 4 * P) P = even;
-            } else {
-                // Measured on the long-context and MQA-end workloads: about
-                // 85% of the SMs, each unit split evenly, beats every SM with
-                // uneven splits (fewer partials, HBM still saturated).
-                const long long even = units * ((P * 85 / 100) / units);
-                if (even >= units && 5 * even >= 4 * P) P = even;
-            }
-        }
-        // First sequence whose tiles reach past lo, and the tiles before it.
-        const long long lo = (long long)blockIdx.x * total / P;
-        long long pre = 0;
-        int bstart = p.B;
-        long long prestart = total;
-        bool found = (long long)blockIdx.x >= P;
-        auto find = [&](int b0, long long v) {
-            const long long incl = scan_add(v);
-            const unsigned hit = __ballot_sync(0xffffffffu, b0 + lane < p.B && pre + incl > lo);
-            if (hit) {
-                const int src = __ffs(hit) - 1;
-                bstart = b0 + src;
-                prestart = pre + __shfl_sync(0xffffffffu, incl - v, src);
-                found = true;
-            } else {
-                pre += __shfl_sync(0xffffffffu, incl, 31);
-            }
-        };
-#pragma unroll
-        for (int k = 0; k < kCached; ++k)
-            if (!found && k * 32 < p.B) find(k * 32, cached[k]);
-        for (int b0 = kCached * 32; !found && b0 < p.B; b0 += 32) find(b0, tiles_times_g(b0 + lane));
-        if (lane == 0) {
-            shared_ll[0] = total;
-            shared_ll[1] = bstart;
-            shared_ll[2] = prestart;
-            shared_ll[3] = P;
-        }
-    }
+    // Warp 0: this CTA's share of the tiles (plan_share).
+    if (warp == 0) plan_share<kTileTokens>(p, lane, shared_ll);
     __syncthreads();
     pdl_launch_dependents();
 

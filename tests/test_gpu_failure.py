@@ -18,8 +18,13 @@ from gpu_helpers import compare, make_inputs, run_gpu, to_device_bf16
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("H,G,sq", [(32, 8, 1), (64, 8, 4)], ids=["one-row-tile", "two-row-tiles"])
-def test_expired_wait_is_reported_and_the_context_survives(monkeypatch, H, G, sq):
+@pytest.mark.parametrize("H,G,sq,tc", [(32, 8, 1, "1"), (64, 8, 4, "1"), (64, 8, 4, "0")],
+                         ids=["one-row-tile", "two-row-tiles-tcgen05", "two-row-tiles-mma-sync"])
+def test_expired_wait_is_reported_and_the_context_survives(monkeypatch, H, G, sq, tc):
+    """Two row tiles on both kernels: the m16n8k16 one (default) and the
+    opt-in tcgen05 one (its MMA warp waits for the missing tile; the CTA frees
+    its tensor memory before returning)."""
+    monkeypatch.setenv("GQA_DECODE_TC", tc)
     B, D, Tmax = 2, 128, 700
     q, k, v, lens = make_inputs(B, sq, H, G, D, Tmax, [700, 650], seed=77 + H)
     dq, dk, dv = to_device_bf16(q), to_device_bf16(k), to_device_bf16(v)
@@ -37,8 +42,9 @@ def test_expired_wait_is_reported_and_the_context_survives(monkeypatch, H, G, sq
     monkeypatch.delenv("GQA_DECODE_DEBUG_SKIP_TILE")
     monkeypatch.delenv("GQA_DECODE_DEBUG_TIMEOUT_MS")
     ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, 1 / math.sqrt(D), threads=8)
-    got_out, got_lse = run_gpu(q, k, v, lens, 1 / math.sqrt(D), device_inputs=(dq, dk, dv, dl))
-    compare(got_out, got_lse, ref_out, ref_lse, what="after timeout")
+    for _ in range(2):   # every SM's tensor memory is allocatable again
+        got_out, got_lse = run_gpu(q, k, v, lens, 1 / math.sqrt(D), device_inputs=(dq, dk, dv, dl))
+        compare(got_out, got_lse, ref_out, ref_lse, what="after timeout")
 
 
 def test_prefill_expired_wait_is_reported_and_the_context_survives(monkeypatch):
