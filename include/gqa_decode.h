@@ -37,7 +37,10 @@
  * KV head, R = (H/G)*sq: up to 32 it runs the split-KV decode kernel, above
  * that the prefill kernel (see gqa_prefill, which also needs scale > 0). The
  * other decode entry points (workspace, plan, append, paged, fp8, no-alloc)
- * take R <= 32.
+ * take R <= 32. With the environment variable GQA_DECODE_TC=1, bf16 decode of
+ * a contiguous cache at D = 128 with 17..32 rows runs on a tcgen05 kernel
+ * instead (same results within the tolerances, same workspace; measured
+ * slower on the MQA-end and ragged workloads, so it is off by default).
  * A row with no visible key (T_b - sq + s < 0) gets out = 0 and lse = -inf.
  *
  * Ownership and ordering: the caller owns every tensor and the stream. All
