@@ -710,6 +710,11 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                     mma_f16_16816(sc[1], a1, e4m3x2_to_f16x2((uint16_t)r3), e4m3x2_to_f16x2((uint16_t)(r3 >> 16)));
                 }
             } else {
+                // Two row tiles: odd k steps accumulate apart from even ones
+                // (summed after the loop), which halves the dependent MMA chains
+                // that bound these warps.
+                constexpr bool kSplitK = MT > 1;
+                float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; ++kk) {
                     const int chunk = kk * 2 + k_half;
@@ -726,8 +731,19 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                         ldsm_x4(qa_base + ((qc ^ (qa_row & 7)) << 4), a_s[0], a_s[1], a_s[2], a_s[3]);
                     }
                     const uint32_t(&a)[4] = kQs ? a_s : qa[kQs ? 0 : kk];
-                    mma_bf16_16816(sc[0], a, b0, b1);
-                    mma_bf16_16816(sc[1], a, b2, b3);
+                    if (kSplitK && (kk & 1)) {
+                        mma_bf16_16816(sd[0], a, b0, b1);
+                        mma_bf16_16816(sd[1], a, b2, b3);
+                    } else {
+                        mma_bf16_16816(sc[0], a, b0, b1);
+                        mma_bf16_16816(sc[1], a, b2, b3);
+                    }
+                }
+                if constexpr (kSplitK) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) sc[j][c] += sd[j][c];
                 }
             }
             const float sscale = KV8 ? p.scale_log2 * ks : p.scale_log2;
