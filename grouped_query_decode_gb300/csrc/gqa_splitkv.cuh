@@ -690,7 +690,11 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                 // rows gives each thread 4 consecutive codes (d = 4q..4q+3 of a
                 // 16-wide k step) of one token, i.e. both B registers of that
                 // step in the k order the Q fragments were given. One x4 load
-                // covers 2 tokens tiles x 2 k steps.
+                // covers 2 tokens tiles x 2 k steps. With two row tiles the odd
+                // k steps accumulate apart (summed after the loop): half-length
+                // MMA chains (one row tile measured slower that way).
+                constexpr bool kSplitK = MT > 1;
+                float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; kk += 2) {
                     const int c8 = kk + (lane >> 4);
@@ -706,8 +710,15 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                     const uint32_t(&a1)[4] = kQs ? a1_s : qa[kQs ? 0 : kk + 1];
                     mma_f16_16816(sc[0], a0, e4m3x2_to_f16x2((uint16_t)r0), e4m3x2_to_f16x2((uint16_t)(r0 >> 16)));
                     mma_f16_16816(sc[1], a0, e4m3x2_to_f16x2((uint16_t)r1), e4m3x2_to_f16x2((uint16_t)(r1 >> 16)));
-                    mma_f16_16816(sc[0], a1, e4m3x2_to_f16x2((uint16_t)r2), e4m3x2_to_f16x2((uint16_t)(r2 >> 16)));
-                    mma_f16_16816(sc[1], a1, e4m3x2_to_f16x2((uint16_t)r3), e4m3x2_to_f16x2((uint16_t)(r3 >> 16)));
+                    float(&s1)[2][4] = kSplitK ? sd : sc;
+                    mma_f16_16816(s1[0], a1, e4m3x2_to_f16x2((uint16_t)r2), e4m3x2_to_f16x2((uint16_t)(r2 >> 16)));
+                    mma_f16_16816(s1[1], a1, e4m3x2_to_f16x2((uint16_t)r3), e4m3x2_to_f16x2((uint16_t)(r3 >> 16)));
+                }
+                if constexpr (kSplitK) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) sc[j][c] += sd[j][c];
                 }
             } else {
                 // Two row tiles: odd k steps accumulate apart from even ones
