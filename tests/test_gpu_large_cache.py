@@ -4,7 +4,8 @@ The device caches are [B=2, G=8, Tmax=2^21, D=128] bf16 (8 GiB each; the last
 unit starts at element 15 * 2^28 > 2^32) and a paged pool whose pages in use
 sit above element 2^31. They are allocated with torch.empty: only the valid
 rows are written, the rest holds whatever the memory held (NaN included),
-which the kernels must never let into a result. The oracle runs on small
+which the kernels must never let into a result (decode, fused append, paged
+decode, and a prefill chunk on the tcgen05 kernel). The oracle runs on small
 host copies (Tmax = 1024) holding the same valid rows -- it reads no entry
 past a sequence's length, so its result is the same.
 """
@@ -106,4 +107,22 @@ def test_paged_pool_with_pages_past_2_31_elements():
     assert gq.gqa_decode_check_error() == gq.GQA_OK
     compare(bf16_to_f64(out), lse.cpu().numpy().astype(np.float64), ref_out, ref_lse, what="paged, big pool")
     del kp, vp
+    torch.cuda.empty_cache()
+
+
+def test_prefill_chunk_over_a_cache_past_2_32_elements():
+    """A 64-token chunk (256 rows per KV head: the tcgen05 prefill kernel)
+    over the same 2^21-token cache."""
+    H, sq = 32, 64
+    q, k, v, lens = make_inputs(B, sq, H, G, D, TMAX_SMALL, LENS, seed=1501)
+    scale = 1 / math.sqrt(D)
+    ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, scale, threads=8)
+    dk, dv = _big_caches(k, v)
+    out = torch.empty(B, sq, H, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, sq, H, dtype=torch.float32, device="cuda")
+    gq.gqa_prefill(to_device_bf16(q), dk, dv, torch.from_numpy(lens).cuda(), scale, out, lse)
+    torch.cuda.synchronize()
+    assert gq.gqa_decode_check_error() == gq.GQA_OK
+    compare(bf16_to_f64(out), lse.cpu().numpy().astype(np.float64), ref_out, ref_lse, what="prefill, big cache")
+    del dk, dv
     torch.cuda.empty_cache()
