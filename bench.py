@@ -107,7 +107,8 @@ def _source_digest() -> str:
 
 def _ncu_traffic(workload: str):
     """DRAM bytes per launch of the split-KV kernel from the committed ncu
-    summary, if it was taken on the current kernel sources."""
+    summary of this exact workload and variant (e.g. "llama3_8b_layer+fp8"),
+    if it was taken on the current kernel sources."""
     path = os.path.join(PROFILES, f"ncu_splitkv_{workload}.md")
     if not os.path.exists(path):
         return None
@@ -495,7 +496,9 @@ def run_gpu(args, cfg):
             "query_tokens_per_s": ws * cfg.B * cfg.sq / (ms_step * 1e-3),
             "tflops": ws * flops / (ms_step * 1e-3) / 1e12,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": _ncu_traffic(cfg.name),
+                         "frac": achieved / peak,
+                         "traffic": _ncu_traffic(_config_dict(cfg, lens, "", append=args.append, paged=args.paged,
+                                                              fp8=args.fp8)["workload"]),
                          "peak_kind": peak_kind, "kernel": "gqa_splitkv_kernel",
                          "duration_us": kernel_ms * 1e3,
                          "duration": f"average over the {args.steps} launches of the timed region "
