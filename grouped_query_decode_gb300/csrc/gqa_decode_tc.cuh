@@ -558,9 +558,10 @@ __global__ void __launch_bounds__(TcShape<D>::kThreads, 1)
                     contributors = 0;
                     for (long long c = cf; c <= cl; ++c) contributors += (c * W / P) < ((c + 1) * W / P) ? 1u : 0u;
                 }
-                const unsigned arrived =
-                    arrive_unit(p.ws_counters + ((size_t)sg.b * p.G + sg.g) * kMaxRowTiles, p.epoch, p.status);
+                unsigned long long* ctr = p.ws_counters + ((size_t)sg.b * p.G + sg.g) * kMaxRowTiles;
+                const unsigned arrived = arrive_unit(ctr, p.epoch, p.status);
                 *last_flag = arrived == contributors ? 1 : 0;
+                if (arrived == contributors) release_unit(ctr);
             }
             if (!sm_sync()) { ok = false; break; }
             if (!*last_flag) continue;

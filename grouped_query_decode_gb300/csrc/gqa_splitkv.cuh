@@ -103,6 +103,13 @@ __device__ __forceinline__ unsigned arrive_unit(unsigned long long* ctr, unsigne
     return 0;
 }
 
+// The arrival that completes a unit's count resets its counter: a launch
+// replayed from a CUDA graph carries the epoch of the call that was captured,
+// so the next replay must find the count at zero (a zero counter matches no
+// epoch, so a call outside a graph restarts it as before). No other CTA of
+// the launch touches the counter after the last arrival.
+__device__ __forceinline__ void release_unit(unsigned long long* ctr) { atomicExch(ctr, 0ull); }
+
 // The CTA holding tile x, and CTA c's share, for the equal partition of W
 // tiles over P CTAs.
 __device__ __forceinline__ long long cta_of_tile(long long x, long long W, long long P) {
@@ -1079,9 +1086,10 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                     for (long long c = cf; c <= cl; ++c)
                         contributors += (c * W / P) < ((c + 1) * W / P) ? 1u : 0u;
                 }
-                const unsigned arrived = arrive_unit(
-                    p.ws_counters + ((size_t)sg.b * p.G + sg.g) * kMaxRowTiles + mt, p.epoch, p.status);
+                unsigned long long* ctr = p.ws_counters + ((size_t)sg.b * p.G + sg.g) * kMaxRowTiles + mt;
+                const unsigned arrived = arrive_unit(ctr, p.epoch, p.status);
                 last_flag[mt] = arrived == contributors ? 1 : 0;
+                if (arrived == contributors) release_unit(ctr);
             }
         }
         mbar_arrive(mbarC);

@@ -81,7 +81,11 @@ extern "C" {
  * the first call that needs more than the stream's buffer holds. Calls on the
  * same stream are ordered; calls on different streams use different buffers.
  * Make one call per stream before capturing that stream into a CUDA graph, so
- * that no allocation happens during capture.
+ * that no allocation happens during capture. A captured call can be replayed
+ * with new contents of the same tensors (values and seq_lens): the plan
+ * depends on the shapes only, and the kernels leave the workspace's arrival
+ * counters at zero after each merge, so every replay starts from a clean
+ * count.
  *
  * q, k_cache, v_cache, seq_lens, out, lse: device pointers, layouts above.
  * scale: multiplier applied to q.k (1/sqrt(D) for the pages' definition).
