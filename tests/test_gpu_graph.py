@@ -172,3 +172,58 @@ def test_prefill_graph_replays():
         ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, scale, threads=8)
         compare(bf16_to_f64(out), lse.cpu().numpy().astype(np.float64), ref_out, ref_lse,
                 what=f"graph replay {rep} prefill")
+
+
+def test_noalloc_entry_graph_replays():
+    """The allocation-free entry (a fixed per-device scratch array) captured and
+    replayed like the others."""
+    B, sq, H, G, D, Tmax = 3, 2, 32, 8, 128, 1500
+    rng = np.random.default_rng(2501)
+    scale = 1 / math.sqrt(D)
+    dq = torch.empty(B, sq, H, D, dtype=torch.bfloat16, device="cuda")
+    dk = torch.empty(B, G, Tmax, D, dtype=torch.bfloat16, device="cuda")
+    dv = torch.empty_like(dk)
+    dl = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, sq, H, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, sq, H, dtype=torch.float32, device="cuda")
+
+    def load(seed):
+        q, k, v, lens = make_inputs(B, sq, H, G, D, Tmax, _lens(rng, B, Tmax, sq), seed=seed)
+        dq.copy_(to_device_bf16(q)); dk.copy_(to_device_bf16(k)); dv.copy_(to_device_bf16(v))
+        dl.copy_(torch.from_numpy(lens))
+        return q, k, v, lens
+
+    load(2600)
+    s = torch.cuda.Stream()
+    with min_tiles(1):
+        g = _graph(lambda: gq.gqa_decode_noalloc(dq, dk, dv, dl, scale, out, lse), s)
+    for rep in range(REPLAYS):
+        q, k, v, lens = load(2601 + rep)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert gq.gqa_decode_check_error() == gq.GQA_OK
+        ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, scale, threads=8)
+        compare(bf16_to_f64(out), lse.cpu().numpy().astype(np.float64), ref_out, ref_lse,
+                what=f"graph replay {rep} noalloc")
+
+
+def test_chained_steps_read_the_previous_steps_output():
+    """Each step's output is the next step's Q. The decode kernel is launched
+    with programmatic dependent launch, so its prologue may overlap the step
+    before it; it must read no input before that step has finished writing."""
+    B, sq, H, G, D, Tmax = 2, 1, 32, 8, 128, 1800
+    scale = 1 / math.sqrt(D)
+    q, k, v, lens = make_inputs(B, sq, H, G, D, Tmax, [1800, 950], seed=2701)
+    dk, dv, dl = to_device_bf16(k), to_device_bf16(v), torch.from_numpy(lens).cuda()
+    bufs = [to_device_bf16(q)] + [torch.empty(B, sq, H, D, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    lse = torch.empty(B, sq, H, dtype=torch.float32, device="cuda")
+    with min_tiles(1):
+        for i in range(4):
+            gq.gqa_decode(bufs[i], dk, dv, dl, scale, bufs[i + 1], lse)
+    torch.cuda.synchronize()
+    assert gq.gqa_decode_check_error() == gq.GQA_OK
+    # Step 4 against the oracle on step 3's actual output (its bf16 bits).
+    q3 = bufs[3].cpu().view(torch.int16).numpy().view(np.uint16)
+    ref_out, ref_lse = oracle.gqa_decode_f64(q3, k, v, lens, scale, threads=8)
+    compare(bf16_to_f64(bufs[4]), lse.cpu().numpy().astype(np.float64), ref_out, ref_lse, what="chained step 4")
