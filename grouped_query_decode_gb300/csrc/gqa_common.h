@@ -16,7 +16,9 @@ constexpr float kRescaleSlack = 8.0f;   // lazy online-softmax rescale threshold
 // contributor state in shared memory); the grid never exceeds it.
 constexpr int kMaxMergeContrib = 180;
 // Units split over at most this many CTAs are merged by each thread in one
-// round of loads; more contributors take the cooperative three-step merge.
+// round of loads (the contributors' values held in registers); more
+// contributors take the cooperative three-step merge. Kernels with room in
+// their register budget take more (KernelShape::kFastMerge).
 constexpr int kFastMerge = 8;
 
 // The tensor-core decode kernel (17..32 rows per KV head, bf16, D = 128):
@@ -116,6 +118,12 @@ struct KernelShape {
     static constexpr int kMaxRegs =
         (65536 / (kAllocWarps * 32)) / 8 * 8 > 255 ? 255 : (65536 / (kAllocWarps * 32)) / 8 * 8;
     static constexpr bool kQInSmem = MT > 1 || kDual;
+    // One-round merges for up to 24 contributors where the register budget
+    // allows (one row tile, bf16, D = 128: 5 warps, up to 255 registers; long
+    // context B = 1 splits units about 19 ways); 8 elsewhere (at D = 64 the
+    // larger merge raised the kernel from 167 to 245 registers and measured
+    // slower on the tiny workload).
+    static constexpr int kFastMerge = (kMaxRegs >= 240 && D == 128) ? 24 : ::gqa::kFastMerge;
     // bf16 at D = 128 with one row tile: with pages shorter than a tile the
     // stage is page-major (one 4-D box per page brings both 64-column blocks
     // of its rows). Two row tiles keep the block-major stage, whose block

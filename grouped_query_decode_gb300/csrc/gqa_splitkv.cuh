@@ -1098,7 +1098,7 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
         if (!last_flag[mt]) continue;
         __threadfence();   // the other contributors' partials are visible from here on
 
-        if (W >= P && cl - cf < kFastMerge) {
+        if (W >= P && cl - cf < KS::kFastMerge) {
             // ---- few contributors (every CTA from cf to cl has a share): each
             // thread merges four columns of one row in a single round of
             // independent loads. Slot 0 is a CTA's first segment: for every
@@ -1112,10 +1112,10 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                 const int rr = item / C4;
                 const int r = mt * 16 + rr;
                 const int c4 = (item % C4) * 4;
-                float mk[kFastMerge], lk[kFastMerge];
-                float4 ok4[kFastMerge];
+                float mk[KS::kFastMerge], lk[KS::kFastMerge];
+                float4 ok4[KS::kFastMerge];
 #pragma unroll
-                for (int k = 0; k < kFastMerge; ++k) {
+                for (int k = 0; k < KS::kFastMerge; ++k) {
                     mk[k] = -INFINITY;
                     lk[k] = 0.f;
                     ok4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1129,11 +1129,11 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                 }
                 float M = mk[0];
 #pragma unroll
-                for (int k = 1; k < kFastMerge; ++k) M = fmaxf(M, mk[k]);
+                for (int k = 1; k < KS::kFastMerge; ++k) M = fmaxf(M, mk[k]);
                 float L = 0.f;
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int k = 0; k < kFastMerge; ++k) {
+                for (int k = 0; k < KS::kFastMerge; ++k) {
                     const float w = (mk[k] == -INFINITY || lk[k] == 0.f) ? 0.f : lk[k] * fast_exp2(mk[k] - M);
                     L += w;
                     acc.x += w * ok4[k].x;
