@@ -13,3 +13,14 @@ if HERE not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Prints the non-gating error figures the GPU tests noted (max-abs error
+    over the RMS of the reference output), if any ran."""
+    helpers = sys.modules.get("gpu_helpers")
+    lines = getattr(helpers, "QUALITY", None)
+    if lines:
+        terminalreporter.section("max-abs error over the RMS of the reference output (not a gate)")
+        for line in lines:
+            terminalreporter.write_line(line)

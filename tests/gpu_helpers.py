@@ -22,6 +22,22 @@ OUT_ATOL = 1e-2
 OUT_RTOL_BF16 = 2.0 ** -8
 LSE_ATOL = 1e-3
 
+# Not a gate: the max-abs error over the RMS of the reference output, which
+# says how close the result is where |out| is small (about 1/sqrt(T) for
+# N(0,1) inputs, so that 1e-2 is a loose bar on long contexts). Tests that
+# compute it add a line here; conftest prints them in the terminal summary.
+QUALITY: list[str] = []
+
+
+def note_quality(what, err, ref_out):
+    ref = np.asarray(ref_out, dtype=np.float64)
+    ref = ref[np.isfinite(ref)]
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    rel = err / rms if rms > 0 else float("nan")
+    QUALITY.append(f"{what}: max-abs {err:.2e}, RMS of out {rms:.2e}, ratio {rel:.2e}")
+    return rel
+
+
 _PAD = 64          # guard elements on each side of an output (keeps 16 B alignment)
 _CANARY_BF16 = 0x7F7F
 _CANARY_F32 = np.float32(-1.2345e29)

@@ -1,0 +1,116 @@
+"""Closed forms at the decode workloads' full sizes, in the launch configuration
+the bench times, checked on EVERY output row (the full-size oracle tests
+compare a sample of rows; these need no oracle). The attention definition
+(softmax of the scaled scores against the KV head g(h) = h / (H/G), times V;
+"GQA analysis", section "Grouped broadcast") fixes both:
+
+- One dominant key per KV head. Keys are N(0,1) except one row t*(b, g),
+  visible to every new token, set to 4 in every dimension. Query rows are
+  constant: 1 + j/8 in every dimension for head j of its group. The dominant
+  score x* = scale * D * 4 * (1 + j/8) beats every other by more than 30
+  (checked below from the keys), so the softmax weight off t* sums to less
+  than 1e-9: out = V[t*] (values of order 1, where the 1e-2 bar is strict) and
+  lse = x*; the kernel's output must round to V[t*] itself. The CTA shares
+  that do not hold t* give partials whose maximum lies tens below the
+  unit's, which the combine must weigh out; heads of different groups see
+  different t*, so a wrong g(h) fails too.
+- Equal keys. Every visible key of unit (b, g) is the same row, so each query
+  row's scores are all equal: out = the mean of V over its visible keys and
+  lse = x + ln(number of visible keys). A partial that the combine dropped,
+  counted twice or weighed wrongly moves lse by ln(1 +- its share of keys).
+
+Cache rows past each sequence's length hold NaN, as in every parity test.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic as syn
+from gpu_helpers import compare, note_quality, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ["llama3_8b_layer", "mqa_end", "long_ctx_b1", "long_ctx_b4", "ragged_sq4"]
+FOUR = int(syn.f32_to_bf16_bits(np.float32(4.0))[0])
+
+
+def _f64(bits):
+    return syn.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def _done():
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_dominant_key_every_row(name):
+    cfg = syn.config_by_name(name)
+    _, k, v, lens = syn.make_inputs(cfg)
+    B, sq, H, G, D = cfg.B, cfg.sq, cfg.H, cfg.G, cfg.D
+    hpg = H // G
+    j = np.arange(H) % hpg
+    q = np.empty((B, sq, H, D), dtype=np.uint16)
+    q[...] = syn.f32_to_bf16_bits((1.0 + j / 8.0).astype(np.float32))[None, None, :, None]
+
+    rng = np.random.default_rng(cfg.seed + 11)
+    vstar = np.empty((B, G, D))
+    worst = 0.0   # largest bound on the weight off t*, over every row
+    for b in range(B):
+        T = int(lens[b])
+        for g in range(G):
+            ts = int(rng.integers(0, T - sq + 1))      # visible to every new token
+            k[b, g, ts] = FOUR
+            vstar[b, g] = _f64(v[b, g, ts])
+            rowsum = syn.bf16_bits_to_f32(k[b, g, :T]).sum(axis=1, dtype=np.float64)
+            rowsum[ts] = -np.inf
+            # smallest gap x* - x_t is at j = 0 (multiplier 1); at most T keys
+            gap = cfg.scale * (4.0 * D - rowsum.max())
+            worst = max(worst, T * math.exp(-gap))
+    assert worst < 1e-9, f"{name}: keys leave weight {worst:.2e} off the dominant key"
+
+    out, lse = run_gpu(q, k, v, lens, cfg.scale)
+    ref_out = np.broadcast_to(np.repeat(vstar, hpg, axis=1)[:, None], (B, sq, H, D))
+    xstar = cfg.scale * D * 4.0 * (1.0 + j / 8.0)
+    ref_lse = np.broadcast_to(xstar[None, None, :], (B, sq, H))
+    err, _ = compare(out, lse, ref_out, ref_lse, what=f"{name} dominant key")
+    note_quality(f"{name} dominant key (every row)", err, ref_out)
+    # Stricter than the bar: V[t*] is a bf16 value and the weight off t* is
+    # below 1e-9, so the fp32 result rounds back to V[t*] itself; allow one
+    # bf16 step (2^-7 |x|), and 1e-6 where V[t*] is near zero.
+    step = np.abs(ref_out) * 2.0 ** -7 + 1e-6
+    assert np.all(np.abs(out - ref_out) <= step), f"{name}: dominant key off by more than one bf16 step"
+    _done()
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_equal_keys_every_row(name):
+    cfg = syn.config_by_name(name)
+    q, k, v, lens = syn.make_inputs(cfg)
+    B, sq, H, G, D = cfg.B, cfg.sq, cfg.H, cfg.G, cfg.D
+    hpg = H // G
+    ref_out = np.empty((B, sq, H, D))
+    ref_lse = np.empty((B, sq, H))
+    qf = _f64(q)
+    for b in range(B):
+        T = int(lens[b])
+        k[b, :, :T] = k[b, :, :1]
+        for g in range(G):
+            vf = _f64(v[b, g, :T])
+            acc = vf[:T - sq + 1].sum(axis=0)
+            k0 = _f64(k[b, g, 0])
+            for s in range(sq):
+                n = T - sq + s + 1                     # keys visible to new token s
+                if s:
+                    acc = acc + vf[n - 1]
+                heads = slice(g * hpg, (g + 1) * hpg)
+                ref_out[b, s, heads] = acc / n
+                ref_lse[b, s, heads] = cfg.scale * (qf[b, s, heads] @ k0) + math.log(n)
+
+    out, lse = run_gpu(q, k, v, lens, cfg.scale)
+    err, _ = compare(out, lse, ref_out, ref_lse, what=f"{name} equal keys")
+    note_quality(f"{name} equal keys (every row)", err, ref_out)
+    _done()
+

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import synthetic as syn
-from gpu_helpers import OUT_ATOL, compare, run_gpu, to_device_bf16
+from gpu_helpers import OUT_ATOL, compare, note_quality, run_gpu, to_device_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -39,6 +39,7 @@ def test_full_size_workload(name):
         ref_lse[r] = l.reshape(nrows)[r]
     err, lerr = compare(out, lse, ref_out, ref_lse, rows=rows, what=name)
     print(f"{name}: sampled max-abs err out {err:.2e} lse {lerr:.2e}")
+    note_quality(f"{name} ({len(rows)} sampled rows)", err, ref_out[rows])
 
     # every row: finite, and inside the per-column range of V over visible keys
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
