@@ -102,22 +102,49 @@ def _stream_handle(stream, device):
     import torch
     if stream is None:
         stream = torch.cuda.current_stream(device)
+    elif hasattr(stream, "device_index") and stream.device_index != device:
+        raise ValueError(f"stream is on cuda:{stream.device_index}, the tensors on cuda:{device}")
     return ctypes.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def _shapes(q, k_cache, v_cache, seq_lens, out, lse):
+def _call(device, fn, *args):
+    """Calls the library with `device` current (it launches on the current
+    device); switches only when another device is current."""
     import torch
-    for name, t, dt in (("q", q, torch.bfloat16), ("k_cache", k_cache, torch.bfloat16),
-                        ("v_cache", v_cache, torch.bfloat16), ("seq_lens", seq_lens, torch.int32),
-                        ("out", out, torch.bfloat16)):
-        if t.dtype != dt:
-            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
-        if not t.is_cuda:
-            raise TypeError(f"{name} must be a CUDA tensor")
-        if not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
-    if lse is not None and (lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous()):
-        raise TypeError("lse must be a contiguous float32 CUDA tensor or None")
+    if torch.cuda.current_device() == device:
+        return fn(*args)
+    with torch.cuda.device(device):
+        return fn(*args)
+
+
+def _check(dev, name, t, dt):
+    """dtype, device (the CUDA device `dev`) and contiguity of one tensor; the
+    device index doubles as the CUDA check (-1 for host tensors)."""
+    if t.dtype != dt:
+        raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+    d = t.get_device()
+    if d < 0:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if d != dev:
+        raise ValueError(f"{name} is on cuda:{d}, q on cuda:{dev}: all tensors must be on one device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _shapes(q, k_cache, v_cache, seq_lens, out, lse):
+    """Checks the tensors of the contiguous-cache entry points (dtype, one
+    CUDA device, contiguity, shapes); returns B, sq, H, G, D, Tmax and the
+    device index."""
+    import torch
+    bf = torch.bfloat16
+    dev = q.get_device()
+    _check(dev, "q", q, bf)
+    _check(dev, "k_cache", k_cache, bf)
+    _check(dev, "v_cache", v_cache, bf)
+    _check(dev, "seq_lens", seq_lens, torch.int32)
+    _check(dev, "out", out, bf)
+    if lse is not None:
+        _check(dev, "lse", lse, torch.float32)
     if q.dim() != 4 or k_cache.dim() != 4:
         raise ValueError("q is [B, sq, H, D] and k_cache [B, G, Tmax, D]")
     B, sq, H, D = q.shape
@@ -128,16 +155,16 @@ def _shapes(q, k_cache, v_cache, seq_lens, out, lse):
         raise ValueError("seq_lens must be [B] and out [B, sq, H, D]")
     if lse is not None and tuple(lse.shape) != (B, sq, H):
         raise ValueError("lse must be [B, sq, H]")
-    return B, sq, H, G, D, Tmax
+    return B, sq, H, G, D, Tmax, dev
 
 
 def gqa_decode(q, k_cache, v_cache, seq_lens, scale, out, lse=None, stream=None):
     """One decode step (library-owned workspace). See include/gqa_decode.h."""
-    B, sq, H, G, D, Tmax = _shapes(q, k_cache, v_cache, seq_lens, out, lse)
-    rc = load().gqa_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                           seq_lens.data_ptr(), float(scale), out.data_ptr(),
-                           None if lse is None else lse.data_ptr(), B, sq, H, G, D, Tmax,
-                           _stream_handle(stream, q.device))
+    B, sq, H, G, D, Tmax, dev = _shapes(q, k_cache, v_cache, seq_lens, out, lse)
+    rc = _call(dev, load().gqa_decode, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+               seq_lens.data_ptr(), float(scale), out.data_ptr(),
+               None if lse is None else lse.data_ptr(), B, sq, H, G, D, Tmax,
+               _stream_handle(stream, dev))
     if rc != GQA_OK:
         raise GQADecodeError(rc, "gqa_decode")
 
@@ -146,11 +173,11 @@ def gqa_prefill(q, k_cache, v_cache, seq_lens, scale, out, lse=None, stream=None
     """Prefill or chunked prefill: the same attention as gqa_decode for any
     number of new tokens sq (no limit on (H/G)*sq), on the tcgen05 kernel.
     The sq new tokens' K/V must already be in the cache; seq_lens counts them."""
-    B, sq, H, G, D, Tmax = _shapes(q, k_cache, v_cache, seq_lens, out, lse)
-    rc = load().gqa_prefill(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                            seq_lens.data_ptr(), float(scale), out.data_ptr(),
-                            None if lse is None else lse.data_ptr(), B, sq, H, G, D, Tmax,
-                            _stream_handle(stream, q.device))
+    B, sq, H, G, D, Tmax, dev = _shapes(q, k_cache, v_cache, seq_lens, out, lse)
+    rc = _call(dev, load().gqa_prefill, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+               seq_lens.data_ptr(), float(scale), out.data_ptr(),
+               None if lse is None else lse.data_ptr(), B, sq, H, G, D, Tmax,
+               _stream_handle(stream, dev))
     if rc != GQA_OK:
         raise GQADecodeError(rc, "gqa_prefill")
 
@@ -159,18 +186,17 @@ def gqa_decode_append(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out, l
                       stream=None):
     """One decode step that first appends the sq new tokens' K/V ([B, sq, G, D]
     bf16) to the caches at positions seq_lens[b] - sq + s, in the same launch."""
-    B, sq, H, G, D, Tmax = _shapes(q, k_cache, v_cache, seq_lens, out, lse)
+    B, sq, H, G, D, Tmax, dev = _shapes(q, k_cache, v_cache, seq_lens, out, lse)
     import torch
     for name, t in (("k_new", k_new), ("v_new", v_new)):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-            raise TypeError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+        _check(dev, name, t, torch.bfloat16)
         if tuple(t.shape) != (B, sq, G, D):
             raise ValueError(f"{name} must be [B, sq, G, D]")
-    rc = load().gqa_decode_append(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
-                                  k_cache.data_ptr(), v_cache.data_ptr(), seq_lens.data_ptr(),
-                                  float(scale), out.data_ptr(),
-                                  None if lse is None else lse.data_ptr(), B, sq, H, G, D, Tmax,
-                                  _stream_handle(stream, q.device))
+    rc = _call(dev, load().gqa_decode_append, q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+               k_cache.data_ptr(), v_cache.data_ptr(), seq_lens.data_ptr(),
+               float(scale), out.data_ptr(),
+               None if lse is None else lse.data_ptr(), B, sq, H, G, D, Tmax,
+               _stream_handle(stream, dev))
     if rc != GQA_OK:
         raise GQADecodeError(rc, "gqa_decode_append")
 
@@ -180,11 +206,11 @@ def gqa_decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale, out, lse
     """One decode step over a paged cache: k_pages/v_pages [num_pages, G,
     page_size, D] bf16, block_table [B, max_pages_per_seq] int32."""
     import torch
+    dev = q.get_device()
     for name, t, dt in (("q", q, torch.bfloat16), ("k_pages", k_pages, torch.bfloat16),
                         ("v_pages", v_pages, torch.bfloat16), ("block_table", block_table, torch.int32),
                         ("seq_lens", seq_lens, torch.int32), ("out", out, torch.bfloat16)):
-        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
-            raise TypeError(f"{name} must be a contiguous {dt} CUDA tensor")
+        _check(dev, name, t, dt)
     B, sq, H, D = q.shape
     num_pages, G, page_size, Dk = k_pages.shape
     if Dk != D or tuple(v_pages.shape) != tuple(k_pages.shape):
@@ -193,13 +219,15 @@ def gqa_decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale, out, lse
         raise ValueError("block_table must be [B, max_pages_per_seq]")
     if tuple(seq_lens.shape) != (B,) or tuple(out.shape) != (B, sq, H, D):
         raise ValueError("seq_lens must be [B] and out [B, sq, H, D]")
-    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, sq, H)):
-        raise ValueError("lse must be float32 [B, sq, H]")
-    rc = load().gqa_decode_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
-                                 block_table.data_ptr(), seq_lens.data_ptr(), float(scale),
-                                 out.data_ptr(), None if lse is None else lse.data_ptr(),
-                                 B, sq, H, G, D, page_size, num_pages, block_table.shape[1],
-                                 _stream_handle(stream, q.device))
+    if lse is not None:
+        _check(dev, "lse", lse, torch.float32)
+        if tuple(lse.shape) != (B, sq, H):
+            raise ValueError("lse must be [B, sq, H]")
+    rc = _call(dev, load().gqa_decode_paged, q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+               block_table.data_ptr(), seq_lens.data_ptr(), float(scale),
+               out.data_ptr(), None if lse is None else lse.data_ptr(),
+               B, sq, H, G, D, page_size, num_pages, block_table.shape[1],
+               _stream_handle(stream, dev))
     if rc != GQA_OK:
         raise GQADecodeError(rc, "gqa_decode_paged")
 
@@ -210,12 +238,12 @@ def gqa_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, seq_lens, scale, out, 
     uint8 e4m3 codes, k_scale/v_scale [B, G, ceil(Tmax/64)] float32 (one scale
     per 64-token block)."""
     import torch
+    dev = q.get_device()
     for name, t, dt in (("q", q, torch.bfloat16), ("k_codes", k_codes, torch.uint8),
                         ("v_codes", v_codes, torch.uint8), ("k_scale", k_scale, torch.float32),
                         ("v_scale", v_scale, torch.float32), ("seq_lens", seq_lens, torch.int32),
                         ("out", out, torch.bfloat16)):
-        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
-            raise TypeError(f"{name} must be a contiguous {dt} CUDA tensor")
+        _check(dev, name, t, dt)
     B, sq, H, D = q.shape
     Bk, G, Tmax, Dk = k_codes.shape
     if (Bk, Dk) != (B, D) or tuple(v_codes.shape) != tuple(k_codes.shape):
@@ -225,12 +253,17 @@ def gqa_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, seq_lens, scale, out, 
         raise ValueError("k_scale / v_scale must be [B, G, ceil(Tmax/64)]")
     if tuple(seq_lens.shape) != (B,) or tuple(out.shape) != (B, sq, H, D):
         raise ValueError("seq_lens must be [B] and out [B, sq, H, D]")
-    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, sq, H)):
-        raise ValueError("lse must be float32 [B, sq, H]")
-    rc = load().gqa_decode_fp8(q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(),
-                               k_scale.data_ptr(), v_scale.data_ptr(), seq_lens.data_ptr(),
-                               float(scale), out.data_ptr(), None if lse is None else lse.data_ptr(),
-                               B, sq, H, G, D, Tmax, _stream_handle(stream, q.device))
+    import torch
+    dev = q.get_device()
+    for name, t, dt in (("q", q, torch.bfloat16), ("k_codes", k_codes, torch.uint8),
+                        ("v_codes", v_codes, torch.uint8), ("k_scale", k_scale, torch.float32),
+                        ("v_scale", v_scale, torch.float32), ("seq_lens", seq_lens, torch.int32),
+                        ("out", out, torch.bfloat16)):
+        _check(dev, name, t, dt)
+    rc = _call(dev, load().gqa_decode_fp8, q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(),
+               k_scale.data_ptr(), v_scale.data_ptr(), seq_lens.data_ptr(),
+               float(scale), out.data_ptr(), None if lse is None else lse.data_ptr(),
+               B, sq, H, G, D, Tmax, _stream_handle(stream, dev))
     if rc != GQA_OK:
         raise GQADecodeError(rc, "gqa_decode_fp8")
 
@@ -238,12 +271,14 @@ def gqa_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, seq_lens, scale, out, 
 def gqa_decode_ex(q, k_cache, v_cache, seq_lens, scale, out, lse, workspace, stream=None):
     """One decode step with a caller-owned workspace (a CUDA uint8 tensor of at
     least gqa_decode_workspace_bytes(...) bytes)."""
-    B, sq, H, G, D, Tmax = _shapes(q, k_cache, v_cache, seq_lens, out, lse)
-    rc = load().gqa_decode_ex(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                              seq_lens.data_ptr(), float(scale), out.data_ptr(),
-                              None if lse is None else lse.data_ptr(), B, sq, H, G, D, Tmax,
-                              workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                              _stream_handle(stream, q.device))
+    B, sq, H, G, D, Tmax, dev = _shapes(q, k_cache, v_cache, seq_lens, out, lse)
+    import torch
+    _check(dev, "workspace", workspace, torch.uint8)
+    rc = _call(dev, load().gqa_decode_ex, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+               seq_lens.data_ptr(), float(scale), out.data_ptr(),
+               None if lse is None else lse.data_ptr(), B, sq, H, G, D, Tmax,
+               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+               _stream_handle(stream, dev))
     if rc != GQA_OK:
         raise GQADecodeError(rc, "gqa_decode_ex")
 
@@ -258,11 +293,11 @@ def gqa_decode_noalloc(q, k_cache, v_cache, seq_lens, scale, out, lse=None, stre
     allocate once running (a pre-reserved memory pool, a framework plugin with
     no allocator, a loop that cannot take cudaMalloc's synchronisation). Calls
     on one device share that array, so calls that overlap on the GPU race."""
-    B, sq, H, G, D, Tmax = _shapes(q, k_cache, v_cache, seq_lens, out, lse)
-    rc = load().gqa_decode_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                                   seq_lens.data_ptr(), float(scale), out.data_ptr(),
-                                   None if lse is None else lse.data_ptr(), B, sq, H, G, D, Tmax,
-                                   _stream_handle(stream, q.device))
+    B, sq, H, G, D, Tmax, dev = _shapes(q, k_cache, v_cache, seq_lens, out, lse)
+    rc = _call(dev, load().gqa_decode_noalloc, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+               seq_lens.data_ptr(), float(scale), out.data_ptr(),
+               None if lse is None else lse.data_ptr(), B, sq, H, G, D, Tmax,
+               _stream_handle(stream, dev))
     if rc != GQA_OK:
         raise GQADecodeError(rc, "gqa_decode_noalloc")
 
@@ -282,5 +317,7 @@ def gqa_decode_plan(B, sq, H, G, D, Tmax, num_sms) -> dict:
 def gqa_decode_check_error(stream=None, device=None) -> int:
     """Synchronises the stream and returns (and clears) the device status."""
     import torch
-    dev = device if device is not None else torch.cuda.current_device()
-    return int(load().gqa_decode_check_error(_stream_handle(stream, dev)))
+    if device is None:
+        device = stream.device_index if hasattr(stream, "device_index") else torch.cuda.current_device()
+    dev = device if isinstance(device, int) else torch.device(device).index
+    return int(_call(dev, load().gqa_decode_check_error, _stream_handle(stream, dev)))

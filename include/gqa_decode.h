@@ -43,6 +43,13 @@
  * slower on the MQA-end and ragged workloads, so it is off by default).
  * A row with no visible key (T_b - sq + s < 0) gets out = 0 and lse = -inf.
  *
+ * Device: every pointer is device memory of the current CUDA device (the one
+ * cudaGetDevice returns in the calling thread) and `stream` belongs to that
+ * device. Like other CUDA libraries, the library does not look up where a
+ * pointer lives: a host pointer or another device's memory is undefined
+ * behaviour. (The Python binding checks that all tensors share one device and
+ * makes it current for the call.)
+ *
  * Ownership and ordering: the caller owns every tensor and the stream. All
  * work is enqueued on `stream` (0 = legacy default stream); no call
  * synchronises the host except gqa_decode_check_error. Inputs must not be

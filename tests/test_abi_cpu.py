@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import grouped_query_decode_gb300 as gq
 
@@ -106,3 +107,31 @@ def test_prefill_argument_checks_need_no_gpu():
     assert call((256, 520, 768, 1024, 1280), (1, 64, 32, 8, 64, 4096)) == gq.GQA_ERR_MISALIGNED
     # 2^31 rows of output would overflow the kernel's 32-bit row numbers
     assert call(good, (1 << 16, 1 << 10, 32, 8, 64, 4096)) == gq.GQA_ERR_UNSUPPORTED
+
+
+def test_binding_refuses_host_tensors_wrong_dtypes_and_shapes():
+    """The Python binding passes raw pointers, so it must refuse what the C
+    side cannot see: host tensors (a host pointer handed to a kernel),
+    another dtype, or shapes that disagree. All of it before any library call."""
+    bf = torch.bfloat16
+    q = torch.zeros(1, 1, 32, 128, dtype=bf)
+    k = torch.zeros(1, 8, 64, 128, dtype=bf)
+    lens = torch.zeros(1, dtype=torch.int32)
+    out = torch.zeros_like(q)
+    for fn in (gq.gqa_decode, gq.gqa_decode_noalloc, gq.gqa_prefill):
+        with pytest.raises(TypeError, match="CUDA tensor"):
+            fn(q, k, k, lens, 0.1, out)
+        with pytest.raises(TypeError, match="must be torch.bfloat16"):
+            fn(q.float(), k, k, lens, 0.1, out)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        gq.gqa_decode_ex(q, k, k, lens, 0.1, out, None, torch.zeros(1 << 20, dtype=torch.uint8))
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        gq.gqa_decode_append(q, torch.zeros(1, 1, 8, 128, dtype=bf), torch.zeros(1, 1, 8, 128, dtype=bf),
+                             k, k, lens, 0.1, out)
+    pages = torch.zeros(4, 8, 16, 128, dtype=bf)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        gq.gqa_decode_paged(q, pages, pages, torch.zeros(1, 4, dtype=torch.int32), lens, 0.1, out)
+    codes = torch.zeros(1, 8, 64, 128, dtype=torch.uint8)
+    sc = torch.ones(1, 8, 1)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        gq.gqa_decode_fp8(q, codes, codes, sc, sc, lens, 0.1, out)
