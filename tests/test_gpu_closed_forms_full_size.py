@@ -114,3 +114,108 @@ def test_equal_keys_every_row(name):
     note_quality(f"{name} equal keys (every row)", err, ref_out)
     _done()
 
+
+
+# ---------------------------------------------------------------- fp8 cache
+# The same two forms over an e4m3 cache with one scale per 64-token block,
+# against the dequantised values (torch's e4m3 decoding of the codes times
+# the block's scale). On one row tile the fp8 kernel runs two groups of
+# consumer warps on alternate tiles, whose states merge in shared memory
+# before the cross-CTA merge: a dominant key sits in one group's state only.
+# The kernel carries V's scale as an fp16 multiplier of P, so the output is
+# checked against the bar only (no one-step bound).
+
+FP8_NAMES = ["llama3_8b_layer", "mqa_end", "long_ctx_b1"]
+
+
+def _dequant_unit(codes, scales, b, g, T):
+    x = torch.from_numpy(np.ascontiguousarray(codes[b, g, :T])).view(torch.float8_e4m3fn).double()
+    s = torch.from_numpy(scales[b, g]).double().repeat_interleave(64)[:T, None]
+    return (x * s).numpy()
+
+
+def _run_fp8(cfg, q, kc, ks, vc, vs, lens):
+    import grouped_query_decode_gb300 as gq
+    from gpu_helpers import bf16_to_f64, to_device_bf16
+    out = torch.empty(cfg.B, cfg.sq, cfg.H, cfg.D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(cfg.B, cfg.sq, cfg.H, dtype=torch.float32, device="cuda")
+    gq.gqa_decode_fp8(to_device_bf16(q), torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda(),
+                      torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda(),
+                      torch.from_numpy(lens).cuda(), cfg.scale, out, lse)
+    torch.cuda.synchronize()
+    assert gq.gqa_decode_check_error() == gq.GQA_OK
+    return bf16_to_f64(out), lse.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("name", FP8_NAMES)
+def test_fp8_dominant_key_every_row(name):
+    cfg = syn.config_by_name(name)
+    _, k, v, lens = syn.make_inputs(cfg)
+    B, sq, H, G, D = cfg.B, cfg.sq, cfg.H, cfg.G, cfg.D
+    hpg = H // G
+    j = np.arange(H) % hpg
+    mult = 1.0 + j / 8.0
+    q = np.empty((B, sq, H, D), dtype=np.uint16)
+    q[...] = syn.f32_to_bf16_bits(mult.astype(np.float32))[None, None, :, None]
+    rng = np.random.default_rng(cfg.seed + 12)
+    tstar = np.empty((B, G), dtype=np.int64)
+    for b in range(B):
+        for g in range(G):
+            tstar[b, g] = int(rng.integers(0, int(lens[b]) - sq + 1))
+            k[b, g, tstar[b, g]] = FOUR
+    kc, ks = syn.fp8_cache(k, lens)
+    vc, vs = syn.fp8_cache(v, lens)
+    del k, v
+
+    ref_out = np.empty((B, sq, H, D))
+    ref_lse = np.empty((B, sq, H))
+    worst = 0.0
+    for b in range(B):
+        T = int(lens[b])
+        for g in range(G):
+            ts = int(tstar[b, g])
+            rowsum = _dequant_unit(kc, ks, b, g, T).sum(axis=1)
+            xs = rowsum[ts]
+            rowsum[ts] = -np.inf
+            worst = max(worst, T * math.exp(-cfg.scale * (xs - rowsum.max())))
+            heads = slice(g * hpg, (g + 1) * hpg)
+            ref_out[b, :, heads] = _dequant_unit(vc, vs, b, g, ts + 1)[ts]
+            ref_lse[b, :, heads] = cfg.scale * xs * mult[heads]
+    assert worst < 1e-9, f"{name}: keys leave weight {worst:.2e} off the dominant key"
+
+    out, lse = _run_fp8(cfg, q, kc, ks, vc, vs, lens)
+    err, _ = compare(out, lse, ref_out, ref_lse, what=f"{name} fp8 dominant key")
+    note_quality(f"{name} fp8 dominant key (every row)", err, ref_out)
+    _done()
+
+
+@pytest.mark.parametrize("name", FP8_NAMES)
+def test_fp8_equal_keys_every_row(name):
+    cfg = syn.config_by_name(name)
+    q, k, v, lens = syn.make_inputs(cfg)
+    B, sq, H, G, D = cfg.B, cfg.sq, cfg.H, cfg.G, cfg.D
+    hpg = H // G
+    for b in range(B):
+        k[b, :, :int(lens[b])] = k[b, :, :1]
+    kc, ks = syn.fp8_cache(k, lens)
+    vc, vs = syn.fp8_cache(v, lens)
+    del k, v
+    qf = _f64(q)
+    ref_out = np.empty((B, sq, H, D))
+    ref_lse = np.empty((B, sq, H))
+    for b in range(B):
+        T = int(lens[b])
+        for g in range(G):
+            kd = _dequant_unit(kc, ks, b, g, T)
+            assert np.array_equal(kd, np.broadcast_to(kd[:1], kd.shape)), "dequantised keys differ"
+            vd = _dequant_unit(vc, vs, b, g, T)
+            heads = slice(g * hpg, (g + 1) * hpg)
+            for s in range(sq):
+                n = T - sq + s + 1
+                ref_out[b, s, heads] = vd[:n].mean(axis=0)
+                ref_lse[b, s, heads] = cfg.scale * (qf[b, s, heads] @ kd[0]) + math.log(n)
+
+    out, lse = _run_fp8(cfg, q, kc, ks, vc, vs, lens)
+    err, _ = compare(out, lse, ref_out, ref_lse, what=f"{name} fp8 equal keys")
+    note_quality(f"{name} fp8 equal keys (every row)", err, ref_out)
+    _done()
