@@ -219,3 +219,56 @@ def test_fp8_equal_keys_every_row(name):
     err, _ = compare(out, lse, ref_out, ref_lse, what=f"{name} fp8 equal keys")
     note_quality(f"{name} fp8 equal keys (every row)", err, ref_out)
     _done()
+
+
+# ------------------------------------------------- periodic keys (causal edge)
+# Key t is 32 e_(t mod D) (one-hot), and the query of new token s of head j is
+# 32 (1 + j/8) e_(p mod D), p = T - sq + s its position. A key scores
+# x = 1024 scale (1 + j/8) (90 or more here) when t = p mod D and exactly 0
+# otherwise, so out = the mean of V over the visible keys t <= p with
+# t = p (mod D), and lse = x + ln(their number). The diagonal key (t = p)
+# is always among them and the next key of the class (p + D) never: any
+# causal off-by-one moves the result. Rows whose first tiles hold no
+# matching key also take the rescale path when the first one arrives.
+
+def _periodic_case(cfg):
+    _, _, v, lens = syn.make_inputs(cfg)
+    B, sq, H, G, D, Tmax = cfg.B, cfg.sq, cfg.H, cfg.G, cfg.D, cfg.Tmax
+    hpg = H // G
+    mult = 1.0 + (np.arange(H) % hpg) / 8.0
+    k = np.full((B, G, Tmax, D), syn.BF16_NAN, dtype=np.uint16)
+    q = np.zeros((B, sq, H, D), dtype=np.uint16)
+    ref_out = np.empty((B, sq, H, D))
+    ref_lse = np.empty((B, sq, H))
+    x = 1024.0 * cfg.scale * mult
+    qvals = syn.f32_to_bf16_bits((32.0 * mult).astype(np.float32))
+    for b in range(B):
+        T = int(lens[b])
+        t = np.arange(T)
+        k[b, :, :T] = 0
+        k[b, :, t, t % D] = int(syn.f32_to_bf16_bits(np.float32(32.0))[0])
+        p = T - sq + np.arange(sq)                     # positions of the new tokens
+        q[b, np.arange(sq)[:, None], np.arange(H)[None, :], (p % D)[:, None]] = qvals[None, :]
+        count = p // D + 1
+        Tp = -(-T // D) * D
+        for g in range(G):
+            vf = np.zeros((Tp, D))
+            vf[:T] = _f64(v[b, g, :T])
+            csum = np.cumsum(vf.reshape(Tp // D, D, D), axis=0)   # [row block, residue, dim]
+            means = csum[p // D, p % D] / count[:, None]          # [sq, D]
+            heads = slice(g * hpg, (g + 1) * hpg)
+            ref_out[b, :, heads] = means[:, None, :]
+            ref_lse[b, :, heads] = x[None, heads] + np.log(count)[:, None]
+    return q, k, v, lens, ref_out, ref_lse
+
+
+@pytest.mark.parametrize("name", NAMES + [c.name for c in syn.PREFILL_CONFIGS])
+def test_periodic_keys_every_row(name):
+    import grouped_query_decode_gb300 as gq
+    cfg = syn.config_by_name(name)
+    q, k, v, lens, ref_out, ref_lse = _periodic_case(cfg)
+    entry = gq.gqa_prefill if cfg.rows > 32 else gq.gqa_decode
+    out, lse = run_gpu(q, k, v, lens, cfg.scale, entry=entry)
+    err, _ = compare(out, lse, ref_out, ref_lse, what=f"{name} periodic keys")
+    note_quality(f"{name} periodic keys (every row)", err, ref_out)
+    _done()
