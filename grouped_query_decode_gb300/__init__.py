@@ -52,6 +52,8 @@ class PlanT(ctypes.Structure):
 def load():
     """Builds (if the sources are newer) and loads libgqa_decode.so."""
     global _lib
+    if _lib is not None:           # every call after the first: no lock
+        return _lib
     with _lock:
         if _lib is None:
             path = _build.build()
