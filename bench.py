@@ -50,6 +50,19 @@ KERNEL_SOURCES = [os.path.join(ROOT, "grouped_query_decode_gb300", "csrc", f) fo
 
 # ------------------------------------------------------------ accounting
 
+def _percentiles_us(ms_list):
+    """p10, median and p90 of per-call event times (ms), in microseconds."""
+    if not ms_list:
+        return None
+    xs = sorted(ms_list)
+
+    def at(f):
+        # nearest rank on the sorted sample
+        return xs[min(len(xs) - 1, max(0, int(round(f * (len(xs) - 1)))))] * 1e3
+
+    return [at(0.10), at(0.50), at(0.90)]
+
+
 def kv_bytes(G: int, D: int, lens, elem_bytes: int = 2) -> int:
     """K and V bytes one decode step must read: 2 (K and V) x sum_b T_b x G x D
     x element size -- the KV-cache sizing formula of "GQA analysis" (section
@@ -84,6 +97,23 @@ def prefill_flops(H: int, D: int, sq: int, lens) -> int:
     """QK^T and PV over the visible (causal) keys only: 2 x 2 flops per key per
     head dimension element per query row."""
     return 4 * H * D * visible_keys(sq, lens)
+
+
+def prefill_launches_per_step(B: int, sq: int, H: int, G: int, Tmax: int, sms: int) -> int:
+    """Kernel launches one gqa_prefill call makes: the prefill kernel, plus the
+    combine kernel when the library splits key ranges. It does that for short
+    chunks whose pairs of 128-row tiles (B*G*ceil(tiles/2) items) cannot fill
+    the SMs: splits = min(sms // items, key_tiles // 2) when 2*items <= sms,
+    at most 32, or GQA_PREFILL_SPLITS when set."""
+    rows = (H // G) * sq
+    items = B * G * ((-(-rows // 128) + 1) // 2)
+    splits = 1
+    if 2 * items <= sms:
+        splits = max(1, min(sms // items, -(-Tmax // 128) // 2))
+    forced = int(os.environ.get("GQA_PREFILL_SPLITS", "0") or 0)
+    if forced > 0:
+        splits = forced
+    return 2 if min(splits, 32) > 1 else 1
 
 
 # --------------------------------------------------------------- helpers
@@ -403,6 +433,7 @@ def run_gpu(args, cfg):
     torch.cuda.synchronize(dev)
     call_ms = [a.elapsed_time(b) for a, b in evs]
     call_ms_mean = statistics.mean(call_ms) if call_ms else float("nan")
+    call_pct = _percentiles_us(call_ms)
     peak, peak_kind = _peaks()
     # One kernel launch per step: its average duration over the timed region
     # is the region's event time / K (launches back to back on one stream).
@@ -504,6 +535,7 @@ def run_gpu(args, cfg):
                          "duration": f"average over the {args.steps} launches of the timed region "
                                      "(CUDA events on the launching stream; one launch per step)",
                          "per_call_us": call_ms_mean * 1e3,
+                         "per_call_p10_p50_p90_us": call_pct,
                          "per_call": f"mean of {n_calls} calls each bracketed by its own events "
                                      "(adds the launch gap that back-to-back launches hide)",
                          "algorithmic_bytes_per_launch": nbytes},
@@ -629,6 +661,19 @@ def run_gpu_prefill(args, cfg):
     ms_step, _ = aggregate_over_ranks(ms_total / args.steps, nbytes, device=dev)
     value = ws * flops / (ms_step * 1e-3) / 1e12
     kernel_ms = ms_total / args.steps
+    launches = prefill_launches_per_step(cfg.B, cfg.sq, cfg.H, cfg.G, cfg.Tmax,
+                                         torch.cuda.get_device_properties(dev).multi_processor_count)
+
+    # Per-call durations (events around each call, same stream).
+    n_calls = min(args.steps, 50)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_calls)]
+    for i, (ea, eb) in enumerate(evs):
+        ea.record(stream)
+        step(i)
+        eb.record(stream)
+    torch.cuda.synchronize(dev)
+    call_ms = [ea.elapsed_time(eb) for ea, eb in evs]
     achieved = flops / (kernel_ms * 1e-3) / 1e12
     peak, peak_kind = _tensor_peak()
 
@@ -678,15 +723,22 @@ def run_gpu_prefill(args, cfg):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
                          "kernel": "gqa_prefill_kernel", "duration_us": kernel_ms * 1e3,
-                         "duration": f"average over the {args.steps} launches of the timed region "
-                                     "(CUDA events on the launching stream; one launch per step)",
+                         "duration": f"average step over the {args.steps} steps of the timed region "
+                                     "(CUDA events on the launching stream; "
+                                     + ("one launch per step)" if launches == 1 else
+                                        "two launches per step: the prefill kernel over split key "
+                                        "ranges, then the combine kernel)"),
+                         "launches_per_step": launches,
+                         "per_call_us": statistics.mean(call_ms) * 1e3 if call_ms else None,
+                         "per_call_p10_p50_p90_us": _percentiles_us(call_ms),
+                         "per_call": f"{n_calls} calls each bracketed by its own events",
                          "algorithmic_flops_per_launch": flops},
             "cpu_baseline": cpu,
             "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "us_per_step": e2e_ms * 1e3,
                     "h2d_bytes_per_step": hq.nbytes + hk.nbytes + hv.nbytes + hl.nbytes,
                     "d2h_bytes_per_step": ho.nbytes + hlse.nbytes},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * launches,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
