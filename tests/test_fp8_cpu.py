@@ -43,3 +43,17 @@ def test_generator_codes_and_scales():
             assert np.all(np.abs(deq[b, :, :T] - x) <= 2.0 ** -4 * np.abs(x) + 2.0 ** -9 * scales.max())
         assert np.all(codes[b, :, T:] == syn.E4M3_NAN)
     assert np.all(scales[2] == 1.0)
+
+
+def test_dequantize_uses_each_64_token_blocks_own_scale():
+    """Every code 0x38 (the value 1.0): the dequantised cache is exactly the
+    scale of each row's 64-token block, per (sequence, KV head), with a
+    ragged last block (Tmax = 150: blocks of 64, 64 and 22 rows)."""
+    B, G, Tmax, D = 2, 3, 150, 16
+    codes = np.full((B, G, Tmax, D), 0x38, dtype=np.uint8)
+    scales = (np.arange(B * G * 3, dtype=np.float32).reshape(B, G, 3) + 1.0) * np.float32(0.25)
+    deq = oracle.dequantize_fp8(codes, scales)
+    for b in range(B):
+        for g in range(G):
+            for t in range(Tmax):
+                assert np.all(deq[b, g, t] == float(scales[b, g, t // 64])), (b, g, t)
