@@ -45,15 +45,32 @@ def test_generator_codes_and_scales():
     assert np.all(scales[2] == 1.0)
 
 
-def test_dequantize_uses_each_64_token_blocks_own_scale():
-    """Every code 0x38 (the value 1.0): the dequantised cache is exactly the
-    scale of each row's 64-token block, per (sequence, KV head), with a
+def _block_scale_pin_holds(dequantize) -> bool:
+    """Every code 0x38 (the value 1.0): the dequantised cache must be exactly
+    the scale of each row's 64-token block, per (sequence, KV head), with a
     ragged last block (Tmax = 150: blocks of 64, 64 and 22 rows)."""
     B, G, Tmax, D = 2, 3, 150, 16
     codes = np.full((B, G, Tmax, D), 0x38, dtype=np.uint8)
     scales = (np.arange(B * G * 3, dtype=np.float32).reshape(B, G, 3) + 1.0) * np.float32(0.25)
-    deq = oracle.dequantize_fp8(codes, scales)
-    for b in range(B):
-        for g in range(G):
-            for t in range(Tmax):
-                assert np.all(deq[b, g, t] == float(scales[b, g, t // 64])), (b, g, t)
+    deq = dequantize(codes, scales)
+    want = np.repeat(scales.astype(np.float64), 64, axis=2)[:, :, :Tmax, None]
+    return deq.shape == codes.shape and bool(np.all(deq == want))
+
+
+def test_dequantize_uses_each_64_token_blocks_own_scale():
+    assert _block_scale_pin_holds(oracle.dequantize_fp8)
+
+
+def test_block_scale_pin_catches_planted_mistakes():
+    """Copies of the dequantiser with a plausible mistake fail the pin:
+    32-token blocks, and the scale of the next KV head."""
+    def blocks_of_32(codes, scales):
+        B, G, Tmax, D = codes.shape
+        per_row = np.repeat(np.asarray(scales, dtype=np.float64), 32, axis=2)[:, :, :Tmax, None]
+        return oracle.e4m3_to_f64(codes) * per_row
+
+    def next_head(codes, scales):
+        return oracle.dequantize_fp8(codes, np.roll(scales, 1, axis=1))
+
+    assert not _block_scale_pin_holds(blocks_of_32)
+    assert not _block_scale_pin_holds(next_head)
