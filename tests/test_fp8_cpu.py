@@ -66,8 +66,9 @@ def test_block_scale_pin_catches_planted_mistakes():
     32-token blocks, and the scale of the next KV head."""
     def blocks_of_32(codes, scales):
         B, G, Tmax, D = codes.shape
-        per_row = np.repeat(np.asarray(scales, dtype=np.float64), 32, axis=2)[:, :, :Tmax, None]
-        return oracle.e4m3_to_f64(codes) * per_row
+        sc = np.asarray(scales, dtype=np.float64)
+        idx = np.minimum(np.arange(Tmax) // 32, sc.shape[2] - 1)
+        return oracle.e4m3_to_f64(codes) * sc[:, :, idx, None]
 
     def next_head(codes, scales):
         return oracle.dequantize_fp8(codes, np.roll(scales, 1, axis=1))
