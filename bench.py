@@ -233,6 +233,29 @@ def aggregate_over_ranks(ms_per_step: float, bytes_per_rank: int, device=None):
 
 # ----------------------------------------------------------- CPU oracle
 
+def _cpu_model() -> str:
+    """The host CPU's name from /proc/cpuinfo: "model name" (x86), else the
+    Arm implementer and part numbers, else the machine type."""
+    info = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    key, val = line.split(":", 1)
+                    info.setdefault(key.strip(), val.strip())
+    except OSError:
+        pass
+    if info.get("model name"):
+        return info["model name"]
+    if "CPU part" in info:
+        arm_parts = {"0xd4f": "Neoverse V2", "0xd40": "Neoverse V1", "0xd0c": "Neoverse N1",
+                     "0xd49": "Neoverse N2"}
+        part = info["CPU part"].lower()
+        return f"Arm {arm_parts.get(part, 'part ' + part)} (implementer {info.get('CPU implementer', '?')})"
+    import platform
+    return platform.machine() or "unknown"
+
+
 def time_oracle(cfg, q, k, v, lens, budget_s: float, max_reps: int | None = None):
     """Times the oracle (as it stands) over the whole step's rows, split over
     the host's cores; repeats the step until about budget_s of wall time."""
@@ -274,7 +297,7 @@ def run_reference(args, cfg):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": _config_dict(cfg, lens, l2_note="host memory"),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "cpu_model": _cpu_model()},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }
         print(json.dumps(line), flush=True)
@@ -291,7 +314,8 @@ def run_reference(args, cfg):
         "data": "synthetic", "config": _config_dict(cfg, lens, l2_note="host memory"),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"whole decode step ({cfg.B * cfg.sq * cfg.H} query rows), "
-                                   f"{args.steps} steps"},
+                                   f"{args.steps} steps",
+                         "seconds": sum(times), "cpu_model": _cpu_model()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -514,7 +538,8 @@ def run_gpu(args, cfg):
             tc = statistics.median(times)
             cpu = {"value": nbytes / tc / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                    "sample": f"whole decode step ({cfg.B * cfg.sq * cfg.H} query rows) x "
-                             f"{len(times)} repetitions, median"}
+                             f"{len(times)} repetitions, median",
+                   "seconds": sum(times), "cpu_model": _cpu_model()}
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -710,8 +735,10 @@ def run_gpu_prefill(args, cfg):
     if rank == 0:
         cpu = None
         if ws == 1 and not args.no_cpu_baseline:
+            t_cpu = time.perf_counter()
             rate, threads, sample = time_oracle_prefill(cfg, q, k, v, lens, args.cpu_budget_s)
-            cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample}
+            cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample,
+                   "seconds": time.perf_counter() - t_cpu, "cpu_model": _cpu_model()}
         line = {
             "metric": "prefill attention TFLOP/s (causal keys only) at 1 GPU", "value": value,
             "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
