@@ -179,10 +179,14 @@ int gqa_decode_fp8(const void* q, const void* k_codes, const void* v_codes, cons
  * chunked prefill has the earlier chunks' K/V in the cache as well.
  *
  * The products run on the tcgen05 tensor cores (bf16 inputs, fp32
- * accumulation in tensor memory, probabilities rounded to bf16 for P.V). No
- * workspace: one CTA computes each 128-row tile of one (sequence, KV head)
- * over its whole key range. Asynchronous on `stream`; a bounded device-side
- * wait that expires is reported by gqa_decode_check_error().
+ * accumulation in tensor memory, probabilities rounded to bf16 for P.V). One
+ * CTA computes each pair of 128-row tiles of one (sequence, KV head) over its
+ * key range. When those pairs cannot fill the GPU (short chunks), each pair's
+ * key range is shared by several CTAs that write partial results to a
+ * library-owned workspace (per device and stream, as for gqa_decode; make one
+ * call per stream before capturing it into a CUDA graph), and a second kernel
+ * merges them. Asynchronous on `stream`; a bounded device-side wait that
+ * expires is reported by gqa_decode_check_error().
  */
 int gqa_prefill(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
                 float scale, void* out, float* lse, int B, int sq, int H, int G, int D, int Tmax,
@@ -190,9 +194,9 @@ int gqa_prefill(const void* q, const void* k_cache, const void* v_cache, const i
 
 /*
  * Bytes of device workspace gqa_decode_ex needs for these sizes on the current
- * device: two partial-result slots (O[R][D], running max m[R], sum l[R]) per
- * split-KV CTA plus the per-sequence tile prefix sums. Returns 0 for
- * unsupported arguments.
+ * device: one 64-bit arrival counter per (sequence, KV head, 16-row tile),
+ * then two partial-result slots (O[R][D] normalised by its own sum, running
+ * max m[R], sum l[R]) per split-KV CTA. Returns 0 for unsupported arguments.
  */
 size_t gqa_decode_workspace_bytes(int B, int sq, int H, int G, int D, int Tmax);
 
