@@ -55,6 +55,30 @@ def test_fp8_scales_act_per_block():
     compare(out, lse, ref_out, ref_lse, what="fp8 per-block scales")
 
 
+@pytest.mark.parametrize("H,G", [(32, 8), (64, 2)], ids=["one-row-tile", "two-row-tiles"])
+def test_fp8_zero_block_scales(H, G):
+    """A block scale of 0 (an all-zero block, as a caller may store it): a
+    zero K scale makes that block's scores exactly 0, a zero V scale its
+    values 0, including in the first block of a unit and on a unit's every
+    block."""
+    B, sq, D, Tmax = 3, 1, 128, 256
+    q, k, v, lens = make_inputs(B, sq, H, G, D, Tmax, [256, 200, 130], seed=822 + H)
+    kc, ks = syn.fp8_cache(k, lens)
+    vc, vs = syn.fp8_cache(v, lens)
+    last = G - 1
+    ks[0, 0, 0] = 0.0          # first block of a unit
+    vs[0, 0, 0] = 0.0
+    vs[1, last, 2] = 0.0       # a later block
+    ks[1, 0, 1] = 0.0
+    vs[2, last, :] = 0.0       # every block of a unit: out = 0 there
+    ref_out, ref_lse = oracle.gqa_decode_fp8_f64(q, kc, vc, ks, vs, lens, 0.09)
+    with min_tiles(1):
+        out, lse = _run_fp8(q, kc, vc, ks, vs, lens, 0.09)
+    compare(out, lse, ref_out, ref_lse, what=f"fp8 zero block scales H={H} G={G}")
+    hpg = H // G
+    assert np.all(out[2, :, last * hpg:(last + 1) * hpg] == 0.0)
+
+
 def test_fp8_rejects_head_dim_64():
     q, k, v, lens = make_inputs(1, 1, 8, 2, 64, 64, [64], seed=821)
     kc = torch.zeros(1, 2, 64, 64, dtype=torch.uint8, device="cuda")
