@@ -205,3 +205,24 @@ def test_decode_with_more_than_32_rows_per_kv_head(B, sq, H, G, D, lens):
     ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, scale, threads=8)
     out, lse = run_gpu(q, k, v, lens, scale)
     compare(out, lse, ref_out, ref_lse, what=f"decode R={(H // G) * sq}")
+
+
+@pytest.mark.parametrize("sq,H,G,ragged", [(1, 8, 2, True), (4, 16, 2, True), (1, 8, 2, False)],
+                         ids=["one-row-tile", "two-row-tiles", "equal-lengths"])
+def test_more_than_256_sequences(sq, H, G, ragged):
+    """300 sequences: the work partition keeps the first 256 lengths in
+    registers and reads the rest again; shares must start and end at the
+    right sequence past that point too. Equal lengths take the rule that
+    shrinks the grid to a whole number of units per CTA (600 units)."""
+    B, D, Tmax = 300, 64, 96
+    if ragged:
+        lens = syn.uniform_int(5150 + sq, syn.STREAM_LENS, B, 0, Tmax)
+    else:
+        lens = np.full(B, 64, dtype=np.int32)
+    q, k, v, lens = make_inputs(B, sq, H, G, D, Tmax, lens, seed=5160 + sq + int(ragged))
+    scale = 1 / math.sqrt(D)
+    ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, scale, threads=8)
+    for mt in (1, None):
+        with min_tiles(mt):
+            out, lse = run_gpu(q, k, v, lens, scale)
+        compare(out, lse, ref_out, ref_lse, what=f"B=300 sq={sq} ragged={ragged} min_tiles={mt}")
