@@ -17,6 +17,12 @@ roofline = the split-KV kernel (the step's only launch): its average duration
            against the measured HBM copy bandwidth
 cpu_baseline = the fp64 CPU oracle (test infrastructure) on the host cores
 
+Prefill workloads (--workload prefill_* / chunked_prefill_*) run gqa_prefill
+instead and report TFLOP/s over the visible (causal) keys against the measured
+bf16 tensor rate; a short chunk whose key ranges are split is two launches per
+step (prefill kernel, then the combine). --fp8, --paged N and --append time the
+other decode entry points on the same workload.
+
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 on its own GPU (the path has no exchange step); timing is the max over ranks.
 """
