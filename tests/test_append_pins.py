@@ -10,22 +10,52 @@ import synthetic as syn
 from oracle_pins import _bits, _f64, make_case
 
 
-def test_new_rows_land_before_the_length_and_nothing_else_moves():
+def _placement_pin_holds(append) -> bool:
+    """Exactly the sq positions that end at T_b (those >= 0) change, in order,
+    and nothing else: worked out by hand for T = 12, 5, 1 and sq = 2."""
     B, sq, H, G, D, Tmax = 3, 2, 4, 2, 8, 12
     q, k, v, lens = make_case(B, sq, H, G, D, Tmax, [12, 5, 1], seed=50)
     kn = syn.normal_bf16(51, 1, (B, sq, G, D))
     vn = syn.normal_bf16(51, 2, (B, sq, G, D))
-    k2, v2 = oracle.append_f64(k, v, kn, vn, lens)
+    k2, v2 = append(k, v, kn, vn, lens)
     changed = np.zeros((B, Tmax), dtype=bool)
     for b in range(B):
         for t in range(Tmax):
             if not (np.array_equal(k2[b, :, t], k[b, :, t]) and np.array_equal(v2[b, :, t], v[b, :, t])):
                 changed[b, t] = True
-    # exactly the sq positions that end at T_b (those >= 0), nothing else
-    assert changed[0].nonzero()[0].tolist() == [10, 11]
-    assert changed[1].nonzero()[0].tolist() == [3, 4]
-    assert changed[2].nonzero()[0].tolist() == [0]
-    assert np.array_equal(k2[2, :, 0], kn[2, 1]) and np.array_equal(v2[2, :, 0], vn[2, 1])
+    return (changed[0].nonzero()[0].tolist() == [10, 11] and changed[1].nonzero()[0].tolist() == [3, 4]
+            and changed[2].nonzero()[0].tolist() == [0]
+            and np.array_equal(k2[1, :, 3], kn[1, 0]) and np.array_equal(v2[1, :, 4], vn[1, 1])
+            and np.array_equal(k2[2, :, 0], kn[2, 1]) and np.array_equal(v2[2, :, 0], vn[2, 1]))
+
+
+def test_new_rows_land_before_the_length_and_nothing_else_moves():
+    assert _placement_pin_holds(oracle.append_f64)
+
+
+def test_placement_pin_catches_planted_mistakes():
+    """Copies of the append with a plausible mistake fail the pin: one slot
+    late, the new tokens in reverse order, and K and V swapped."""
+    def make(pos, order=lambda s, sq: s, swap=False):
+        def append(k_cache, v_cache, k_new, v_new, seq_lens):
+            k = np.array(k_cache, copy=True)
+            v = np.array(v_cache, copy=True)
+            B, G, Tmax, D = k.shape
+            sq = k_new.shape[1]
+            for b in range(B):
+                for s in range(sq):
+                    t = pos(int(seq_lens[b]), sq, s)
+                    if 0 <= t < Tmax:
+                        src = order(s, sq)
+                        k[b, :, t, :] = (v_new if swap else k_new)[b, src]
+                        v[b, :, t, :] = (k_new if swap else v_new)[b, src]
+            return k, v
+        return append
+
+    assert _placement_pin_holds(make(lambda T, sq, s: T - sq + s))            # the right one
+    assert not _placement_pin_holds(make(lambda T, sq, s: T - sq + s + 1))
+    assert not _placement_pin_holds(make(lambda T, sq, s: T - sq + s, order=lambda s, sq: sq - 1 - s))
+    assert not _placement_pin_holds(make(lambda T, sq, s: T - sq + s, swap=True))
 
 
 def test_a_new_token_attends_to_itself():
