@@ -5,23 +5,30 @@
 
 One step is one gqa_decode call (one split-KV kernel launch, LSE merge included)
 over the whole workload -- every sequence, every query head, one layer. The
-default workload is
-the Llama-3-8B-shaped layer (B=16, H=32, G=8, D=128, T=4096). Inputs are seeded
-synthetic N(0,1) bf16 tensors from the synthetic/ generator.
+default workload is the largest one that fits one GPU: ragged multi-token
+decode (B=64, sq=4 causal, H=64, G=8, D=128, lengths uniform in [512, 32768] in
+a 32768-token cache). Inputs are seeded synthetic N(0,1) bf16 tensors from the
+synthetic/ generator.
 
-value    = algorithmic bytes per step / device time per step (GB/s, all ranks)
+value    = algorithmic bytes per step / device time per step (GB/s, all ranks);
+           the K timed launches are enqueued behind a device-side spin, so the
+           events time back-to-back device work, not the binding's call rate
 e2e      = the same with the step's inputs copied from pinned host memory and its
            outputs copied back inside the timed region
 roofline = the split-KV kernel (the step's only launch): its average duration
            over the timed region, CUDA events on the launching stream,
            against the measured HBM copy bandwidth
-cpu_baseline = the fp64 CPU oracle (test infrastructure) on the host cores
+cpu_baseline = the fp64 CPU oracle (test infrastructure) on the host cores,
+           over a bounded sample of the workload's sequences
+workloads = every other full-size decode workload (Llama-3-8B-shaped layer, MHA
+           and MQA ends, long context at B = 1 and 4), timed in the same run by
+           the same method (--workloads none|NAME,... changes the set)
 
 Prefill workloads (--workload prefill_* / chunked_prefill_*) run gqa_prefill
 instead and report TFLOP/s over the visible (causal) keys against the measured
 bf16 tensor rate; a short chunk whose key ranges are split is two launches per
 step (prefill kernel, then the combine). --fp8, --paged N and --append time the
-other decode entry points on the same workload.
+other decode entry points on the same workloads.
 
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 on its own GPU (the path has no exchange step); timing is the max over ranks.
@@ -47,11 +54,11 @@ if ROOT not in sys.path:
 import synthetic as syn  # noqa: E402
 
 METRIC = "decode-attention µs/step and achieved HBM GB/s (% of GB300 peak) at 1 GPU"
-DEFAULT_WORKLOAD = "llama3_8b_layer"
+DEFAULT_WORKLOAD = "ragged_sq4"
 PROFILES = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = [os.path.join(ROOT, "grouped_query_decode_gb300", "csrc", f) for f in
                   ("gqa_splitkv.cuh", "gqa_device.cuh", "gqa_common.h", "ptx.cuh", "gqa_launch_impl.cuh",
-                   "gqa_decode_tc.cuh", "tcgen05.cuh", "api.cu")]
+                   "api.cu")]
 
 
 # ------------------------------------------------------------ accounting
@@ -308,7 +315,11 @@ def run_reference(args, cfg):
         }
         print(json.dumps(line), flush=True)
         return 0
-    nbytes = algorithmic_bytes(cfg.B, cfg.sq, cfg.H, cfg.G, cfg.D, lens)
+    # Each step is the oracle over a bounded sample of the batch (the whole
+    # batch where one step stays within the sample's budget).
+    n = _oracle_sample(cfg, lens)
+    q, k, v, lens = q[:n], k[:n], v[:n], lens[:n]
+    nbytes = algorithmic_bytes(n, cfg.sq, cfg.H, cfg.G, cfg.D, lens)
     time_oracle(cfg, q, k, v, lens, 0, max_reps=max(1, args.warmup))
     times, threads = time_oracle(cfg, q, k, v, lens, 0, max_reps=args.steps)
     t = sum(times) / len(times)
@@ -319,8 +330,8 @@ def run_reference(args, cfg):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": _config_dict(cfg, lens, l2_note="host memory"),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                         "sample": f"whole decode step ({cfg.B * cfg.sq * cfg.H} query rows), "
-                                   f"{args.steps} steps",
+                         "sample": f"sequences 0..{n - 1} of {cfg.B} ({n * cfg.sq * cfg.H} query rows, "
+                                   f"{nbytes} algorithmic bytes) per step, {args.steps} steps",
                          "seconds": sum(times), "cpu_model": _cpu_model()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -337,89 +348,139 @@ def _config_dict(cfg, lens, l2_note, append=False, paged=0, fp8=False):
 
 # ------------------------------------------------------------ GPU arm
 
-def run_gpu(args, cfg):
+# Full-size decode workloads timed in the same run as the headline line, each
+# by the same method, into its "workloads" map (the headline's own workload is
+# left out of the map). The tiny workload is launch-bound and not among them.
+MAP_WORKLOADS = ("llama3_8b_layer", "long_ctx_b1", "long_ctx_b4", "mha_end", "mqa_end", "ragged_sq4")
+
+
+def _variant_name(cfg, append=False, paged=0, fp8=False) -> str:
+    return (cfg.name + ("+append" if append else "") + (f"+paged{paged}" if paged else "")
+            + ("+fp8" if fp8 else ""))
+
+
+class DecodeWorkload:
+    """Device tensors of one decode workload (and entry-point variant) and its
+    step: one call over the whole batch. The K/V caches rotate over enough
+    copies that their footprint is at least 4x L2, so no step finds its K/V
+    left in L2 by the step before."""
+
+    def __init__(self, cfg, dev, append=False, paged=0, fp8=False, keep_host=False):
+        import torch
+
+        import grouped_query_decode_gb300 as gq
+
+        self.gq = gq
+        self.cfg, self.dev = cfg, dev
+        self.append, self.paged, self.fp8 = append, paged, fp8
+        self.name = _variant_name(cfg, append, paged, fp8)
+        q, k, v, lens = syn.make_inputs(cfg, tail_bits=syn.BF16_ZERO)
+        self.lens = lens
+        self.nbytes = algorithmic_bytes(cfg.B, cfg.sq, cfg.H, cfg.G, cfg.D, lens)
+        self.flops = algorithmic_flops(cfg.sq, cfg.H, cfg.D, lens)
+
+        def to_dev(bits):
+            return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+        self.to_dev = to_dev
+        props = torch.cuda.get_device_properties(dev)
+        self.l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+        self.cache_bytes = 2 * k.nbytes
+        self.copies = copies = max(2, math.ceil(4 * self.l2 / self.cache_bytes))
+        self.dq = to_dev(q)
+        self.dl = torch.from_numpy(lens).to(dev)
+        self.out = torch.empty(cfg.B, cfg.sq, cfg.H, cfg.D, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(cfg.B, cfg.sq, cfg.H, dtype=torch.float32, device=dev)
+        self.host_q, self.host_kv = q, None
+        if fp8:
+            # The same caches as e4m3 codes with one fp32 scale per 64-token block.
+            kc, ksc = syn.fp8_cache(k, lens, tail_code=0)
+            vc, vsc = syn.fp8_cache(v, lens, tail_code=0)
+            self.sets = [(torch.from_numpy(kc).to(dev), torch.from_numpy(vc).to(dev),
+                          torch.from_numpy(ksc).to(dev), torch.from_numpy(vsc).to(dev))
+                         for _ in range(copies)]
+            self.nbytes += (kv_bytes(cfg.G, cfg.D, lens, elem_bytes=1)    # 1-byte codes ...
+                            - kv_bytes(cfg.G, cfg.D, lens)                  # ... instead of bf16
+                            + 2 * 4 * int(sum(-(-int(t) // 64) for t in lens)) * cfg.G)  # block scales
+            if keep_host:
+                self.host_kv = (kc, vc, ksc, vsc)
+        elif paged:
+            # The same logical caches laid out in pages, one paged copy per
+            # rotation slot, each with its own block table.
+            self.sets = []
+            for c in range(copies):
+                kp, vp, table = syn.paginate(k, v, lens, paged, seed=cfg.seed + 100 + c,
+                                             fill_bits=syn.BF16_ZERO)
+                self.sets.append((to_dev(kp), to_dev(vp), torch.from_numpy(table).to(dev)))
+                if c == 0 and keep_host:
+                    self.host_kv = (kp, vp, table)
+            self.nbytes += sum(-(-int(t) // paged) for t in lens) * 4     # block-table entries read
+        else:
+            self.sets = [(to_dev(k), to_dev(v)) for _ in range(copies)]
+            if keep_host:
+                self.host_kv = (k, v)
+        if append:
+            # Fused append: each step also writes the sq new tokens' K/V rows.
+            self.dkn = to_dev(syn.normal_bf16(cfg.seed, 11, (cfg.B, cfg.sq, cfg.G, cfg.D)))
+            self.dvn = to_dev(syn.normal_bf16(cfg.seed, 12, (cfg.B, cfg.sq, cfg.G, cfg.D)))
+            self.nbytes += 2 * 2 * (cfg.B * cfg.sq * cfg.G * cfg.D * 2)   # new rows read + written
+        self.host_bf16 = (k, v) if keep_host else None
+
+    def l2_note(self) -> str:
+        return (f"inputs larger than L2: {self.copies} rotating K/V copies of "
+                f"{self.cache_bytes >> 20} MiB vs {self.l2 >> 20} MiB L2")
+
+    def call(self, stream, kv):
+        gq, cfg = self.gq, self.cfg
+        if self.fp8:
+            kc, vc, ks, vs = kv
+            gq.gqa_decode_fp8(self.dq, kc, vc, ks, vs, self.dl, cfg.scale, self.out, self.lse, stream=stream)
+        elif self.paged:
+            kp, vp, tb = kv
+            gq.gqa_decode_paged(self.dq, kp, vp, tb, self.dl, cfg.scale, self.out, self.lse, stream=stream)
+        elif self.append:
+            gq.gqa_decode_append(self.dq, self.dkn, self.dvn, kv[0], kv[1], self.dl, cfg.scale, self.out,
+                                 self.lse, stream=stream)
+        else:
+            gq.gqa_decode(self.dq, kv[0], kv[1], self.dl, cfg.scale, self.out, self.lse, stream=stream)
+
+    def step(self, i, stream):
+        self.call(stream, self.sets[i % self.copies])
+
+
+def _spin(host_us_per_call: float, calls: int):
+    """Keeps the stream busy on the device for about as long as the host takes
+    to enqueue `calls` more calls (capped at 0.2 s), so that the calls
+    enqueued behind it run back to back: the events around them then time
+    the device's work, not the binding's call rate. Spins on the SM clock
+    (torch's sleep kernel), counted at 2.1 GHz, at least the maximum SM clock."""
+    import torch
+    us = min(2e5, 20.0 + 1.25 * host_us_per_call * calls)
+    torch.cuda._sleep(int(us * 2100))
+
+
+def time_steps(step, steps: int, warmup: int, dev, stream, gpu_index: int, ws: int):
+    """W untimed warm-up steps, then exactly `steps` timed steps on `stream`
+    between two CUDA events, bracketed by barrier + synchronize; then the same
+    number (at most 200) of calls each between its own events. The host
+    enqueues each timed run behind a device-side spin (_spin). nvidia-smi
+    samples the clocks meanwhile. Returns (ms per step, per-call ms list,
+    clocks summary)."""
     import torch
     import torch.distributed as dist
 
     import grouped_query_decode_gb300 as gq
 
-    ws, rank, local = _dist()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if ws > 1:
-        dist.init_process_group("nccl", device_id=dev)
-
-    q, k, v, lens = syn.make_inputs(cfg, tail_bits=syn.BF16_ZERO)
-    nbytes = algorithmic_bytes(cfg.B, cfg.sq, cfg.H, cfg.G, cfg.D, lens)
-    flops = algorithmic_flops(cfg.sq, cfg.H, cfg.D, lens)
-
-    def to_dev(bits):
-        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
-
-    props = torch.cuda.get_device_properties(dev)
-    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
-    cache_bytes = 2 * k.nbytes
-    copies = max(2, math.ceil(4 * l2 / cache_bytes))
-    dq = to_dev(q)
-    dl = torch.from_numpy(lens).to(dev)
-    dks = [to_dev(k) for _ in range(copies)]
-    dvs = [to_dev(v) for _ in range(copies)]
-    out = torch.empty(cfg.B, cfg.sq, cfg.H, cfg.D, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(cfg.B, cfg.sq, cfg.H, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    if args.append:
-        # Fused append: each step also writes the sq new tokens' K/V rows.
-        dkn = to_dev(syn.normal_bf16(cfg.seed, 11, (cfg.B, cfg.sq, cfg.G, cfg.D)))
-        dvn = to_dev(syn.normal_bf16(cfg.seed, 12, (cfg.B, cfg.sq, cfg.G, cfg.D)))
-        nbytes += 2 * 2 * (cfg.B * cfg.sq * cfg.G * cfg.D * 2)   # new rows read + written
-
-    if args.fp8:
-        # The same caches as e4m3 codes with one fp32 scale per 64-token block.
-        kc, ksc = syn.fp8_cache(k, lens, tail_code=0)
-        vc, vsc = syn.fp8_cache(v, lens, tail_code=0)
-        fp8_sets = [(torch.from_numpy(kc).to(dev), torch.from_numpy(vc).to(dev),
-                     torch.from_numpy(ksc).to(dev), torch.from_numpy(vsc).to(dev))
-                    for _ in range(copies)]
-        host_fp8 = (kc, vc, ksc, vsc)
-        del dks[:], dvs[:]
-        nbytes -= kv_bytes(cfg.G, cfg.D, lens)                        # bf16 K/V ...
-        nbytes += kv_bytes(cfg.G, cfg.D, lens, elem_bytes=1)          # ... are 1-byte codes
-        nbytes += 2 * 4 * int(sum(-(-int(t) // 64) for t in lens)) * cfg.G   # block scales read
-
-    if args.paged:
-        # The same logical caches laid out in pages, one paged copy per
-        # rotation slot, each with its own block table.
-        paged = []
-        for c in range(copies):
-            kp, vp, table = syn.paginate(k, v, lens, args.paged, seed=cfg.seed + 100 + c,
-                                         fill_bits=syn.BF16_ZERO)
-            paged.append((to_dev(kp), to_dev(vp), torch.from_numpy(table).to(dev)))
-            if c == 0:
-                host_paged = (kp, vp, table)
-        del dks[:], dvs[:]
-        nbytes += sum(-(-int(t) // args.paged) for t in lens) * 4     # block-table entries read
-
-    def step(i):
-        c = i % copies
-        if args.fp8:
-            kc_, vc_, ks_, vs_ = fp8_sets[c]
-            gq.gqa_decode_fp8(dq, kc_, vc_, ks_, vs_, dl, cfg.scale, out, lse, stream=stream)
-        elif args.paged:
-            kp_, vp_, tb_ = paged[c]
-            gq.gqa_decode_paged(dq, kp_, vp_, tb_, dl, cfg.scale, out, lse, stream=stream)
-        elif args.append:
-            gq.gqa_decode_append(dq, dkn, dvn, dks[c], dvs[c], dl, cfg.scale, out, lse, stream=stream)
-        else:
-            gq.gqa_decode(dq, dks[c], dvs[c], dl, cfg.scale, out, lse, stream=stream)
-
-    for i in range(max(3, args.warmup)):
+    host_us = []
+    for i in range(max(3, warmup)):
+        t0 = time.perf_counter()
         step(i)
+        host_us.append((time.perf_counter() - t0) * 1e6)
     torch.cuda.synchronize(dev)
     assert gq.gqa_decode_check_error(stream) == gq.GQA_OK
+    call_us = statistics.median(host_us[1:]) if len(host_us) > 1 else host_us[0]
 
-    # Timed region: exactly K steps, bracketed by barrier + synchronize.
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(gpu_index)
     sampler.start()
     time.sleep(0.15)
     if ws > 1:
@@ -428,8 +489,9 @@ def run_gpu(args, cfg):
     t_wall0 = time.perf_counter()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    _spin(call_us, steps)
     e0.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         step(i)
     e1.record(stream)
     torch.cuda.synchronize(dev)
@@ -450,132 +512,182 @@ def run_gpu(args, cfg):
     clocks = sampler.summary()
     clocks["window"] = "timed region" if t_wall >= 0.6 else "timed region + untimed tail of the same step"
 
-    ms_step, value = aggregate_over_ranks(ms_total / args.steps, nbytes, device=dev)
-
-    # Per-call durations (events around each call, same stream) for the roofline.
-    n_calls = min(args.steps, 200) if args.steps > 0 else 0
+    # Per-call durations: events around each call, enqueued behind a spin too.
+    n_calls = min(steps, 200) if steps > 0 else 0
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n_calls)]
+    _spin(call_us, n_calls)
     for i, (a, b) in enumerate(evs):
         a.record(stream)
         step(i)
         b.record(stream)
     torch.cuda.synchronize(dev)
-    call_ms = [a.elapsed_time(b) for a, b in evs]
-    call_ms_mean = statistics.mean(call_ms) if call_ms else float("nan")
-    call_pct = _percentiles_us(call_ms)
-    peak, peak_kind = _peaks()
-    # One kernel launch per step: its average duration over the timed region
-    # is the region's event time / K (launches back to back on one stream).
-    kernel_ms = ms_total / args.steps
-    achieved = nbytes / (kernel_ms * 1e-3) / 1e9
     assert gq.gqa_decode_check_error(stream) == gq.GQA_OK
+    return ms_total / steps, [a.elapsed_time(b) for a, b in evs], clocks, call_us
 
-    # End to end: inputs from pinned host memory, outputs back, every step.
+
+def _roofline_entry(wl, ms_step: float, call_ms, peak: float) -> dict:
+    achieved = wl.nbytes / (ms_step * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "kernel": "gqa_splitkv_kernel", "duration_us": ms_step * 1e3,
+            "per_call_us": statistics.mean(call_ms) * 1e3 if call_ms else None,
+            "per_call_p10_p50_p90_us": _percentiles_us(call_ms),
+            "algorithmic_bytes_per_launch": wl.nbytes,
+            "traffic": _ncu_traffic(wl.name)}
+
+
+def _oracle_sample(cfg, lens, flop_budget: float = 2e10) -> int:
+    """Sequences of the oracle's bounded sample: the first n of the batch, n
+    as large as keeps one sampled step within flop_budget (about half a second
+    of the fp64 oracle on 16 host cores)."""
+    per_seq = [4 * cfg.sq * cfg.H * cfg.D * int(t) for t in lens]
+    n, acc = 0, 0
+    for f in per_seq:
+        if n > 0 and acc + f > flop_budget:
+            break
+        acc += f
+        n += 1
+    return n
+
+
+def run_gpu(args, cfg):
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = _peaks()
+    variant = dict(append=args.append, paged=args.paged, fp8=args.fp8)
+
+    wl = DecodeWorkload(cfg, dev, keep_host=True, **variant)
+    ms_step, call_ms, clocks, host_call_us = time_steps(lambda i: wl.step(i, stream), args.steps, args.warmup,
+                                                        dev, stream, local, ws)
+    ms_step, value = aggregate_over_ranks(ms_step, wl.nbytes, device=dev)
+    roof = _roofline_entry(wl, ms_step, call_ms, peak)
+    roof.update({
+        "peak_kind": peak_kind,
+        "duration": f"average over the {args.steps} launches of the timed region (CUDA events on the "
+                    "launching stream; one launch per step; the launches are enqueued behind a device-side "
+                    "spin, so no step waits for the host)",
+        "per_call": f"{len(call_ms)} calls each between its own events (also enqueued behind a spin)",
+        "host_us_per_call": host_call_us,
+    })
+
+    # End to end through the public API: inputs from pinned host memory to the
+    # device, the call, outputs back, every step, all inside the timed region.
+    q = wl.host_q
     hq = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hl = torch.from_numpy(wl.lens).pin_memory()
     if args.fp8:
-        hk = torch.from_numpy(host_fp8[0]).pin_memory()
-        hv = torch.from_numpy(host_fp8[1]).pin_memory()
-        hks = torch.from_numpy(host_fp8[2]).pin_memory()
-        hvs = torch.from_numpy(host_fp8[3]).pin_memory()
-        e2e_k, e2e_v, e2e_ks, e2e_vs = fp8_sets[0]
+        hkv = [torch.from_numpy(x).pin_memory() for x in wl.host_kv]
     elif args.paged:
-        hk = torch.from_numpy(host_paged[0].view(np.int16)).view(torch.bfloat16).pin_memory()
-        hv = torch.from_numpy(host_paged[1].view(np.int16)).view(torch.bfloat16).pin_memory()
-        htab = torch.from_numpy(host_paged[2]).pin_memory()
-        e2e_k, e2e_v, e2e_t = paged[0]
+        kp, vp, table = wl.host_kv
+        hkv = [torch.from_numpy(kp.view(np.int16)).view(torch.bfloat16).pin_memory(),
+               torch.from_numpy(vp.view(np.int16)).view(torch.bfloat16).pin_memory(),
+               torch.from_numpy(table).pin_memory()]
     else:
-        hk = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).pin_memory()
-        hv = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
-        e2e_k, e2e_v = dks[0], dvs[0]
-    hl = torch.from_numpy(lens).pin_memory()
-    ho = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
-    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    e2e_steps = max(3, min(args.steps, 20))
-
+        hkv = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in wl.host_kv]
+    dkv = wl.sets[0]
+    ho = torch.empty(wl.out.shape, dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty(wl.lse.shape, dtype=torch.float32).pin_memory()
     if args.append:
-        hkn = dkn.cpu().pin_memory()
-        hvn = dvn.cpu().pin_memory()
+        hkn = wl.dkn.cpu().pin_memory()
+        hvn = wl.dvn.cpu().pin_memory()
 
     def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        e2e_k.copy_(hk, non_blocking=True)
-        e2e_v.copy_(hv, non_blocking=True)
-        dl.copy_(hl, non_blocking=True)
-        if args.fp8:
-            e2e_ks.copy_(hks, non_blocking=True)
-            e2e_vs.copy_(hvs, non_blocking=True)
-            gq.gqa_decode_fp8(dq, e2e_k, e2e_v, e2e_ks, e2e_vs, dl, cfg.scale, out, lse, stream=stream)
-        elif args.paged:
-            e2e_t.copy_(htab, non_blocking=True)
-            gq.gqa_decode_paged(dq, e2e_k, e2e_v, e2e_t, dl, cfg.scale, out, lse, stream=stream)
-        elif args.append:
-            dkn.copy_(hkn, non_blocking=True)
-            dvn.copy_(hvn, non_blocking=True)
-            gq.gqa_decode_append(dq, dkn, dvn, e2e_k, e2e_v, dl, cfg.scale, out, lse, stream=stream)
-        else:
-            gq.gqa_decode(dq, e2e_k, e2e_v, dl, cfg.scale, out, lse, stream=stream)
-        ho.copy_(out, non_blocking=True)
-        hlse.copy_(lse, non_blocking=True)
+        wl.dq.copy_(hq, non_blocking=True)
+        for d, h in zip(dkv, hkv):
+            d.copy_(h, non_blocking=True)
+        wl.dl.copy_(hl, non_blocking=True)
+        if args.append:
+            wl.dkn.copy_(hkn, non_blocking=True)
+            wl.dvn.copy_(hvn, non_blocking=True)
+        wl.call(stream, dkv)
+        ho.copy_(wl.out, non_blocking=True)
+        hlse.copy_(wl.lse, non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize(dev)
     if ws > 1:
         dist.barrier()
+    e2e_steps = max(3, min(args.steps, 20))
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for _ in range(e2e_steps):
         e2e_step()
     b.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms, e2e_value = aggregate_over_ranks(a.elapsed_time(b) / e2e_steps, nbytes, device=dev)
-    h2d = hq.nbytes + hk.nbytes + hv.nbytes + hl.nbytes + (htab.nbytes if args.paged else 0)
-    if args.fp8:
-        h2d += hks.nbytes + hvs.nbytes
+    e2e_ms, e2e_value = aggregate_over_ranks(a.elapsed_time(b) / e2e_steps, wl.nbytes, device=dev)
+    h2d = hq.nbytes + hl.nbytes + sum(h.nbytes for h in hkv)
     if args.append:
         h2d += hkn.nbytes + hvn.nbytes
     d2h = ho.nbytes + hlse.nbytes
+    del hq, hl, hkv, ho, hlse, dkv
 
-    line = None
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        k, v = wl.host_bf16
+        n = _oracle_sample(cfg, wl.lens)
+        sub_bytes = algorithmic_bytes(n, cfg.sq, cfg.H, cfg.G, cfg.D, wl.lens[:n])
+        times, threads = time_oracle(cfg, q[:n], k[:n], v[:n], wl.lens[:n], args.cpu_budget_s)
+        tc = statistics.median(times)
+        cpu = {"value": sub_bytes / tc / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": (f"sequences 0..{n - 1} of {cfg.B} (every head and new token: "
+                          f"{n * cfg.sq * cfg.H} query rows, {sub_bytes} algorithmic bytes) x "
+                          f"{len(times)} repetitions, median"),
+               "seconds": sum(times), "cpu_model": _cpu_model()}
+    config = _config_dict(cfg, wl.lens, l2_note=wl.l2_note(), **variant)
+    nbytes, flops, name = wl.nbytes, wl.flops, wl.name
+    del wl
+    torch.cuda.empty_cache()
+
+    # The other full-size decode workloads, same variant, same method.
+    names = [n for n in MAP_WORKLOADS if n != cfg.name] if args.workloads == "default" else \
+        ([] if args.workloads == "none" else [n for n in args.workloads.split(",") if n])
+    workloads = {}
+    for wname in names:
+        wcfg = syn.config_by_name(wname)
+        w = DecodeWorkload(wcfg, dev, **variant)
+        w_ms, w_calls, w_clocks, _ = time_steps(lambda i: w.step(i, stream), args.steps, args.warmup,
+                                                 dev, stream, local, ws)
+        w_ms, w_value = aggregate_over_ranks(w_ms, w.nbytes, device=dev)
+        entry = _roofline_entry(w, w_ms, w_calls, peak)
+        workloads[w.name] = {
+            "us_per_step": w_ms * 1e3, "value": w_value, "unit": "GB/s", "frac": entry["frac"],
+            "per_call_p10_p50_p90_us": entry["per_call_p10_p50_p90_us"],
+            "algorithmic_bytes_per_step": w.nbytes, "traffic": entry["traffic"],
+            "gpu_launches": args.steps,
+            "config": {k: getattr(wcfg, k) for k in ("B", "sq", "H", "G", "D", "Tmax")} |
+                      {"sum_T": int(np.sum(w.lens)), "l2": w.l2_note()},
+            "clocks": w_clocks,
+        }
+        del w
+        torch.cuda.empty_cache()
+
     if rank == 0:
-        cpu = None
-        if ws == 1 and not args.no_cpu_baseline:
-            times, threads = time_oracle(cfg, q, k, v, lens, args.cpu_budget_s)
-            tc = statistics.median(times)
-            cpu = {"value": nbytes / tc / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                   "sample": f"whole decode step ({cfg.B * cfg.sq * cfg.H} query rows) x "
-                             f"{len(times)} repetitions, median",
-                   "seconds": sum(times), "cpu_model": _cpu_model()}
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "us_per_step": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": _config_dict(cfg, lens, append=args.append, paged=args.paged, fp8=args.fp8,
-                                   l2_note=f"inputs larger than L2: {copies} rotating "
-                                                       f"K/V copies of {cache_bytes >> 20} MiB vs "
-                                                       f"{l2 >> 20} MiB L2"),
+            "config": config,
             "query_tokens_per_s": ws * cfg.B * cfg.sq / (ms_step * 1e-3),
             "tflops": ws * flops / (ms_step * 1e-3) / 1e12,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak,
-                         "traffic": _ncu_traffic(_config_dict(cfg, lens, "", append=args.append, paged=args.paged,
-                                                              fp8=args.fp8)["workload"]),
-                         "peak_kind": peak_kind, "kernel": "gqa_splitkv_kernel",
-                         "duration_us": kernel_ms * 1e3,
-                         "duration": f"average over the {args.steps} launches of the timed region "
-                                     "(CUDA events on the launching stream; one launch per step)",
-                         "per_call_us": call_ms_mean * 1e3,
-                         "per_call_p10_p50_p90_us": call_pct,
-                         "per_call": f"mean of {n_calls} calls each bracketed by its own events "
-                                     "(adds the launch gap that back-to-back launches hide)",
-                         "algorithmic_bytes_per_launch": nbytes},
+            "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s",
                     "us_per_step": e2e_ms * 1e3,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps,
             "clocks": clocks,
+            "workloads": workloads,
+            "workloads_note": ("every other full-size decode workload, timed in this run by the same method "
+                               f"({args.warmup} warm-up and {args.steps} timed steps, CUDA events, inputs "
+                               "larger than L2); value in GB/s of algorithmic bytes, frac of the same peak"),
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -653,58 +765,12 @@ def run_gpu_prefill(args, cfg):
         c = i % copies
         gq.gqa_prefill(dq, dks[c], dvs[c], dl, cfg.scale, out, lse, stream=stream)
 
-    for i in range(max(3, args.warmup)):
-        step(i)
-    torch.cuda.synchronize(dev)
-    assert gq.gqa_decode_check_error(stream) == gq.GQA_OK
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.15)
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    t_wall0 = time.perf_counter()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    if ws > 1:
-        dist.barrier()
-    t_wall = time.perf_counter() - t_wall0
-    ms_total = e0.elapsed_time(e1)
-    t_tail = time.perf_counter()
-    i = 0
-    while time.perf_counter() - t_tail < max(0.0, 0.6 - t_wall):
-        step(i)
-        i += 1
-        if i % 64 == 0:
-            torch.cuda.synchronize(dev)
-    torch.cuda.synchronize(dev)
-    sampler.stop()
-    clocks = sampler.summary()
-    clocks["window"] = "timed region" if t_wall >= 0.6 else "timed region + untimed tail of the same step"
-    assert gq.gqa_decode_check_error(stream) == gq.GQA_OK
-
-    ms_step, _ = aggregate_over_ranks(ms_total / args.steps, nbytes, device=dev)
+    kernel_ms, call_ms, clocks, _ = time_steps(step, args.steps, args.warmup, dev, stream, local, ws)
+    ms_step, _ = aggregate_over_ranks(kernel_ms, nbytes, device=dev)
     value = ws * flops / (ms_step * 1e-3) / 1e12
-    kernel_ms = ms_total / args.steps
     launches = prefill_launches_per_step(cfg.B, cfg.sq, cfg.H, cfg.G, cfg.Tmax,
                                          torch.cuda.get_device_properties(dev).multi_processor_count)
-
-    # Per-call durations (events around each call, same stream).
-    n_calls = min(args.steps, 50)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n_calls)]
-    for i, (ea, eb) in enumerate(evs):
-        ea.record(stream)
-        step(i)
-        eb.record(stream)
-    torch.cuda.synchronize(dev)
-    call_ms = [ea.elapsed_time(eb) for ea, eb in evs]
+    n_calls = len(call_ms)
     achieved = flops / (kernel_ms * 1e-3) / 1e12
     peak, peak_kind = _tensor_peak()
 
@@ -798,6 +864,9 @@ def main(argv=None):
                     help="time gqa_decode_fp8 on the same caches as e4m3 codes with block scales")
     ap.add_argument("--append", action="store_true",
                     help="time gqa_decode_append (new K/V rows written in the same launch)")
+    ap.add_argument("--workloads", default="default",
+                    help="decode workloads also timed into the line's 'workloads' map: 'default' (every "
+                         "other full-size decode workload), 'none', or a comma-separated list of names")
     args = ap.parse_args(argv)
     cfg = syn.config_by_name(args.workload)
     if args.impl == "reference":
