@@ -80,6 +80,8 @@ def load():
             lib.gqa_decode_plan.restype = i32
             lib.gqa_decode_check_error.argtypes = [vp]
             lib.gqa_decode_check_error.restype = i32
+            lib.gqa_decode_release_workspace.argtypes = [vp]
+            lib.gqa_decode_release_workspace.restype = i32
             lib.gqa_decode_last_cuda_error.argtypes = []
             lib.gqa_decode_last_cuda_error.restype = i32
             lib.gqa_decode_strerror.argtypes = [i32]
@@ -133,6 +135,16 @@ def _check(dev, name, t, dt):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _check_lse(dev, lse, B, sq, H):
+    """lse is optional; when given it is float32 [B, sq, H] on q's device."""
+    import torch
+    if lse is None:
+        return
+    _check(dev, "lse", lse, torch.float32)
+    if tuple(lse.shape) != (B, sq, H):
+        raise ValueError("lse must be [B, sq, H]")
+
+
 def _shapes(q, k_cache, v_cache, seq_lens, out, lse):
     """Checks the tensors of the contiguous-cache entry points (dtype, one
     CUDA device, contiguity, shapes); returns B, sq, H, G, D, Tmax and the
@@ -145,8 +157,6 @@ def _shapes(q, k_cache, v_cache, seq_lens, out, lse):
     _check(dev, "v_cache", v_cache, bf)
     _check(dev, "seq_lens", seq_lens, torch.int32)
     _check(dev, "out", out, bf)
-    if lse is not None:
-        _check(dev, "lse", lse, torch.float32)
     if q.dim() != 4 or k_cache.dim() != 4:
         raise ValueError("q is [B, sq, H, D] and k_cache [B, G, Tmax, D]")
     B, sq, H, D = q.shape
@@ -155,8 +165,7 @@ def _shapes(q, k_cache, v_cache, seq_lens, out, lse):
         raise ValueError("k_cache / v_cache must be [B, G, Tmax, D] with q's B and D")
     if tuple(seq_lens.shape) != (B,) or tuple(out.shape) != (B, sq, H, D):
         raise ValueError("seq_lens must be [B] and out [B, sq, H, D]")
-    if lse is not None and tuple(lse.shape) != (B, sq, H):
-        raise ValueError("lse must be [B, sq, H]")
+    _check_lse(dev, lse, B, sq, H)
     return B, sq, H, G, D, Tmax, dev
 
 
@@ -221,10 +230,7 @@ def gqa_decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale, out, lse
         raise ValueError("block_table must be [B, max_pages_per_seq]")
     if tuple(seq_lens.shape) != (B,) or tuple(out.shape) != (B, sq, H, D):
         raise ValueError("seq_lens must be [B] and out [B, sq, H, D]")
-    if lse is not None:
-        _check(dev, "lse", lse, torch.float32)
-        if tuple(lse.shape) != (B, sq, H):
-            raise ValueError("lse must be [B, sq, H]")
+    _check_lse(dev, lse, B, sq, H)
     rc = _call(dev, load().gqa_decode_paged, q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
                block_table.data_ptr(), seq_lens.data_ptr(), float(scale),
                out.data_ptr(), None if lse is None else lse.data_ptr(),
@@ -255,13 +261,7 @@ def gqa_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, seq_lens, scale, out, 
         raise ValueError("k_scale / v_scale must be [B, G, ceil(Tmax/64)]")
     if tuple(seq_lens.shape) != (B,) or tuple(out.shape) != (B, sq, H, D):
         raise ValueError("seq_lens must be [B] and out [B, sq, H, D]")
-    import torch
-    dev = q.get_device()
-    for name, t, dt in (("q", q, torch.bfloat16), ("k_codes", k_codes, torch.uint8),
-                        ("v_codes", v_codes, torch.uint8), ("k_scale", k_scale, torch.float32),
-                        ("v_scale", v_scale, torch.float32), ("seq_lens", seq_lens, torch.int32),
-                        ("out", out, torch.bfloat16)):
-        _check(dev, name, t, dt)
+    _check_lse(dev, lse, B, sq, H)
     rc = _call(dev, load().gqa_decode_fp8, q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(),
                k_scale.data_ptr(), v_scale.data_ptr(), seq_lens.data_ptr(),
                float(scale), out.data_ptr(), None if lse is None else lse.data_ptr(),
@@ -302,6 +302,17 @@ def gqa_decode_noalloc(q, k_cache, v_cache, seq_lens, scale, out, lse=None, stre
                _stream_handle(stream, dev))
     if rc != GQA_OK:
         raise GQADecodeError(rc, "gqa_decode_noalloc")
+
+
+def gqa_decode_release_workspace(stream=None, device=None) -> None:
+    """Frees the library-owned workspace of (device, stream) after the work
+    queued on the stream; the next call on that stream allocates again."""
+    import torch
+    if device is None:
+        device = stream.device_index if hasattr(stream, "device_index") else torch.cuda.current_device()
+    rc = _call(device, load().gqa_decode_release_workspace, _stream_handle(stream, device))
+    if rc != GQA_OK:
+        raise GQADecodeError(rc, "gqa_decode_release_workspace")
 
 
 def gqa_decode_workspace_bytes(B, sq, H, G, D, Tmax) -> int:

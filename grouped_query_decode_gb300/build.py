@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(PKG, "libgqa_decode.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
 SOURCES = ["api.cu", "api_noalloc.cu", "splitkv_d64.cu", "splitkv_d128.cu", "splitkv_d128_fp8.cu",
-           "decode_tc.cu", "prefill.cu"]
+           "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -163,14 +163,14 @@ void debug_knobs(unsigned long long* timeout_ns, int* skip_tile) {
     *skip_tile = k ? std::atoi(k) : -1;
 }
 
-// GQA_DECODE_TC=1 runs 17..32-row bf16 decode on the tcgen05 kernel instead
-// of the m16n8k16 split-KV kernel. It is opt-in: measured on the MQA end
-// (95 against 60 us) and the ragged sq = 4 workload (847 against 694 us), its
-// per-tile rate is higher but each segment boundary, first tile and merge
-// waits on global round trips behind the copy stream.
-bool tc_decode_enabled() {
-    const char* s = std::getenv("GQA_DECODE_TC");
-    return s && s[0] == '1';
+// Test hook: GQA_DECODE_DEBUG_EPOCH=n gives every call the same counter tag n,
+// as the replays of a call captured in a CUDA graph have, so that a test can
+// check that a call that timed out leaves the arrival counters clean for the
+// next call with the same tag.
+unsigned long long call_epoch() {
+    const char* s = std::getenv("GQA_DECODE_DEBUG_EPOCH");
+    const long long e = s ? std::atoll(s) : 0;
+    return e > 0 ? (unsigned long long)e & 0xFFFFFFFFFFFFull : next_epoch();
 }
 
 // Grid size override for sweeps of the plan (unset: the heuristic decides).
@@ -257,14 +257,9 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32
         return GQA_ERR_WORKSPACE;
 
     LaunchArgs a;
-    // Two row tiles (17..32 rows), bf16, D = 128, contiguous cache, no fused
-    // append: the tcgen05 kernel, on 128-token tiles.
-    const bool tc = tc_decode_enabled() && !kv8 && D == 128 && plan.row_tiles == 2 && !pg.block_table &&
-                    !k_new;
     const long long slabs = pg.block_table ? (long long)pg.num_pages * G : (long long)B * G;
     const int rows = pg.block_table ? pg.page_size : Tmax;
-    const int box_rows =
-        tc ? kTcTokens : (pg.block_table && pg.page_size < kTileTokens ? pg.page_size : kTileTokens);
+    const int box_rows = pg.block_table && pg.page_size < kTileTokens ? pg.page_size : kTileTokens;
     // Pages shorter than a tile, one row tile: the kernel's stage is
     // page-major and one box per page brings both halves of a bf16 D = 128
     // row (the 4-D view); elsewhere one 3-D box per half (measured as fast).
@@ -279,7 +274,7 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32
     a.p.lse = lse;
     a.p.ws_counters = static_cast<unsigned long long*>(workspace);
     a.p.ws_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws_counter_bytes(B, G));
-    a.p.epoch = next_epoch();
+    a.p.epoch = call_epoch();
     a.p.status = info.status;
     a.p.scale_log2 = scale * 1.4426950408889634f;
     a.p.B = B;
@@ -306,7 +301,7 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32
     a.row_tiles = plan.row_tiles;
     a.pdl = true;
     a.stream = stream;
-    cudaError_t e = tc ? launch_decode_tc(a) : kv8 ? launch_d128_fp8(a) : (D == 64 ? launch_d64(a) : launch_d128(a));
+    cudaError_t e = kv8 ? launch_d128_fp8(a) : (D == 64 ? launch_d64(a) : launch_d128(a));
     if (e != cudaSuccess) return cuda_fail(e);
     return GQA_OK;
 }
@@ -523,6 +518,25 @@ int gqa_decode_check_error(cudaStream_t stream) {
         e = cudaMemcpy(info.status, &zero, sizeof zero, cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return cuda_fail(e);
         if (word & kStatusTimeout) return GQA_ERR_DEVICE_TIMEOUT;
+    }
+    return GQA_OK;
+}
+
+int gqa_decode_release_workspace(cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_workspaces.find({dev, stream});
+    if (it == g_workspaces.end()) return GQA_OK;
+    // Work already queued on the stream may still use the buffer.
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    void* buf = it->second.first;
+    g_workspaces.erase(it);
+    if (buf) {
+        e = cudaFree(buf);
+        if (e != cudaSuccess) return cuda_fail(e);
     }
     return GQA_OK;
 }

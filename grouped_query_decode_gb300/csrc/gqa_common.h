@@ -21,11 +21,6 @@ constexpr int kMaxMergeContrib = 180;
 // their register budget take more (KernelShape::kFastMerge).
 constexpr int kFastMerge = 8;
 
-// The tensor-core decode kernel (17..32 rows per KV head, bf16, D = 128):
-// tokens per K/V tile (its MMAs' M) and the rows it serves (their N).
-constexpr int kTcTokens = 128;
-constexpr int kTcRows = 32;
-
 // Status bits of the per-device status word.
 constexpr unsigned kStatusTimeout = 1u;
 
@@ -109,8 +104,19 @@ struct KernelShape {
     // alternate tiles of each segment (a 16 KB fp8 stage is consumed at the
     // rate of a 32 KB bf16 one otherwise) and merge at the segment's end.
     static constexpr bool kDual = KV8 && MT == 1;
-    static constexpr int kGroups = kDual ? 2 : 1;
-    static constexpr int kConsumerWarps = kSlices * MT * kGroups;
+    // bf16 caches: "wide" slices. The four consumer warps of a row tile are
+    // two groups that take alternate tiles of each segment, and a warp reads
+    // 32 of its tile's 64 tokens (group = slice / 2, half = slice % 2): each Q
+    // fragment then serves four n8 token tiles, and the softmax's reductions,
+    // the stage wait and the arrival are paid once per 32 tokens. The four
+    // warps still merge as four slices at the end of each segment.
+    static constexpr bool kWide = !KV8;
+    static constexpr int kGroups = (kDual || kWide) ? 2 : 1;
+    // Tokens of a stage one consumer warp reads.
+    static constexpr int kWarpTokens = kWide ? 32 : 16;
+    static constexpr int kConsumerWarps = kSlices * MT * (kDual ? 2 : 1);
+    // Consumer warps that read each stage (its "empty" barrier's count).
+    static constexpr int kStageReaders = kConsumerWarps / kGroups;
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;
     // Registers per thread: the 64K register file for one CTA, with warps
     // counted in the allocation steps of 4, in steps of 8 registers, <= 255.
@@ -146,7 +152,17 @@ struct KernelShape {
     static constexpr int kMlBytes = MT * kSlices * 16 * 2 * 4;
     static constexpr int kQBytes = kConsumerWarps * kQBytesPerWarp;
     // fp8 stages are half as large: twice as many keep the same bytes in flight.
-    static constexpr int kStages = KV8 ? 8 : (D == 128 ? (MT == 1 ? 5 : 4) : 8);
+    static constexpr int kStages = KV8 ? 8 : (D == 128 ? (MT == 1 ? 6 : 4) : 8);
+    // With groups on alternate tiles, a warp waits on tile t having read only
+    // every other tile before it. Tile t - kStages, the stage's previous
+    // load, must then be its own group's (read, hence landed, by this warp):
+    // the copies of different stages land in any order, and a stage whose
+    // previous load is still in flight shows the phase two loads back, whose
+    // parity equals tile t's, so the wait would pass before tile t landed.
+    // An even ring keeps tile t - kStages in the warp's own group (across a
+    // segment boundary the segment-end merge barrier has seen every earlier
+    // tile land).
+    static_assert(kStages % kGroups == 0, "the ring depth must be a multiple of the groups");
     // Dual groups: group 1's per-lane state (m, l partials and the O
     // fragments of each slice) for group 0 to merge.
     static constexpr int kGroupBytes = kDual ? kSlices * 32 * (D / 8 * 4 + 4) * 4 : 0;

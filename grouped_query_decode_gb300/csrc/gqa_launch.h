@@ -24,13 +24,6 @@ cudaError_t launch_d64(const LaunchArgs& a);
 cudaError_t launch_d128(const LaunchArgs& a);
 cudaError_t launch_d128_fp8(const LaunchArgs& a);
 
-// The tensor-core decode kernel (bf16, D = 128, 17..32 rows per KV head,
-// contiguous cache; maps with 128-row boxes): same parameters, workspace and
-// grid as the split-KV kernel.
-cudaError_t launch_decode_tc(const LaunchArgs& a);
-int decode_tc_smem_bytes();
-int decode_tc_threads();
-
 // The prefill kernel: one CTA per 128-row tile of one (sequence, KV head).
 struct PrefillLaunchArgs {
     CUtensorMap tm_k;

@@ -116,6 +116,29 @@ __device__ __forceinline__ long long cta_of_tile(long long x, long long W, long 
     return ((x + 1) * P - 1) / W;
 }
 
+// CTAs that hold a share of the unit whose tiles are [ub, ue): with at least
+// one tile per CTA every CTA from the first to the last holder; otherwise the
+// non-empty shares among them are counted.
+__device__ __forceinline__ unsigned unit_contributors(long long ub, long long ue, long long W, long long P) {
+    const long long cf = cta_of_tile(ub, W, P), cl = cta_of_tile(ue - 1, W, P);
+    if (W >= P) return (unsigned)(cl - cf + 1);
+    unsigned n = 0;
+    for (long long c = cf; c <= cl; ++c) n += (c * W / P) < ((c + 1) * W / P) ? 1u : 0u;
+    return n;
+}
+
+// Counts a unit's arrival for row tile mt; the arrival that completes the
+// count resets the counter. Returns true for that (last) arrival.
+__device__ __forceinline__ bool arrive_and_release(const DecodeParams& p, const Segment& s, int mt, long long W,
+                                                   long long P) {
+    unsigned long long* ctr = p.ws_counters + ((size_t)s.b * p.G + s.g) * kMaxRowTiles + mt;
+    const unsigned contributors = unit_contributors(s.ub, s.ue, W, P);
+    const unsigned arrived = arrive_unit(ctr, p.epoch, p.status);
+    if (arrived != contributors) return false;
+    release_unit(ctr);
+    return true;
+}
+
 // Byte offset of row r (0..63), 64-column block bx, in a stage of a cache
 // with P = 2^lp rows per TMA box (P = 64, one box per tile, or the page size
 // of a paged cache with shorter pages): boxes of P rows are laid out one
@@ -420,7 +443,7 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar + 8 * s, 1);
             // Each stage is read by the warps of one group.
-            mbar_init(empty_bar + 8 * s, KS::kConsumerWarps / KS::kGroups);
+            mbar_init(empty_bar + 8 * s, KS::kStageReaders);
         }
         for (int m = 0; m < 4 * MT; ++m) mbar_init(merge_bar + 8 * m, kSlices * 32);
         mbar_init(group_bar, KS::kConsumerWarps * 32);
@@ -470,7 +493,9 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     // ---------------------------------------------------------- consumers
     const int slice = warp % kSlices;
     const int mt = KS::kDual ? 0 : warp / kSlices;
-    const int group = KS::kDual ? warp / kSlices : 0;     // dual groups: 0 or 1
+    // Groups take alternate tiles: the fp8 kernel's dual groups (warps 0-3 and
+    // 4-7), or the two halves of a row tile's warps (wide slices).
+    const int group = KS::kDual ? warp / kSlices : (KS::kWide ? slice >> 1 : 0);
     const int quad = lane & 3;
     const int grp = lane >> 2;
     const int tid_mt = slice * 32 + lane;                   // 0..127 within the row tile
@@ -483,13 +508,18 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     const size_t slot_floats = ws_slot_floats(p.R, D);
     const uint64_t tmo = p.wait_timeout_ns;
 
-    // ldmatrix row addressing inside a stage (bytes from the stage base).
+    // This warp's tokens of a stage: [tok0, tok0 + kWarpTokens).
+    constexpr int WT = KS::kWarpTokens;
+    constexpr int NJ = WT / 8;   // n8 token tiles of the warp's S
+    const int tok0 = KS::kWide ? (slice & 1) * WT : slice * WT;
+    // ldmatrix row addressing inside a stage (bytes from the stage base), for
+    // the warp's first 16 tokens (16 * jj more for the jj-th 16).
     // Q.K^T (B operand, non-transposed): matrix m = lane/8 -> n8 tile (m>>1),
     // k half (m&1); row = token.
-    const int k_tok = slice * 16 + ((lane >> 4) << 3) + (lane & 7);
+    const int k_tok = tok0 + ((lane >> 4) << 3) + (lane & 7);
     const int k_half = (lane >> 3) & 1;
     // P.V (B operand, transposed): matrix m -> d tile (m>>1), token half (m&1).
-    const int v_tok = slice * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
+    const int v_tok = tok0 + (((lane >> 3) & 1) << 3) + (lane & 7);
     const int v_dt = lane >> 4;
     // e4m3 K and V (one byte per element, one 128-byte box row per token):
     // matrix m -> tokens 8*(m&1).., 16-byte chunk + (m>>1).
@@ -499,7 +529,12 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     const int lp = (KS::kPageMajor && p.block_table != nullptr && p.page_size < kTileTokens)
                        ? 31 - __clz(p.page_size) : 6;
     // Block 1 of a row sits 2^(lp+7) bytes after block 0 (stage_off).
-    const uint32_t k_off0 = stage_row_off<KS>(k_tok, 0, lp), v_off0 = stage_row_off<KS>(v_tok, 0, lp);
+    uint32_t k_off0[NJ / 2], v_off0[NJ / 2];
+#pragma unroll
+    for (int jj = 0; jj < NJ / 2; ++jj) {
+        k_off0[jj] = stage_row_off<KS>(k_tok + 16 * jj, 0, lp);
+        v_off0[jj] = stage_row_off<KS>(v_tok + 16 * jj, 0, lp);
+    }
     const uint32_t bx_stride = KS::kPageMajor ? 1u << (lp + 7) : kTileTokens * 128;
 
     uint32_t it_base = 0;      // tiles of this CTA's earlier segments
@@ -508,8 +543,10 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     uint32_t c_parity = 0;     // phases of merge barrier C (partial segments)
     uint32_t d_parity = 0;     // phases of merge barrier D (merges)
     bool failed = false;
+    bool arrived_here = false;   // lane 0 of a row tile's slice 0: this segment's arrival counted
     Segment sg;
     while (!failed && walk.next(sg)) {
+        arrived_here = false;
         // Rows of this warp's 16-row tile: r = j*sq + s (head j of the group,
         // new token s), the row fold of section 7 of "Same GQA, Different
         // Execution Cost Across Backends".
@@ -559,22 +596,35 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             } else {
                 // This warp's 16 Q rows into its own shared-memory copy, 16-byte
                 // chunks swizzled by row so that ldmatrix reads are conflict free.
+                // Every load is issued before the first store: one global round
+                // trip per segment, not one per chunk.
                 unsigned char* qw = q_smem + warp * KS::kQBytesPerWarp;
                 if constexpr (KV8) {
                     // fp16, each 16-wide k step stored as the A fragments of the
                     // e4m3 k order: chunk 2c holds d {0,1,4,5,8,9,12,13} of step
                     // c, chunk 2c+1 d {2,3,6,7,10,11,14,15}.
-                    for (int idx = lane; idx < 16 * (D / 16); idx += 32) {
+                    constexpr int kIters = 16 * (D / 16) / 32;
+                    uint4 qa4[kIters], qb4[kIters];
+#pragma unroll
+                    for (int u = 0; u < kIters; ++u) {
+                        const int idx = lane + 32 * u;
                         const int row = idx / (D / 16), c16 = idx % (D / 16);
                         const int r = mt * 16 + row;
-                        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+                        qa4[u] = make_uint4(0u, 0u, 0u, 0u);
+                        qb4[u] = qa4[u];
                         if (r < p.R) {
                             const int j = r / p.sq, sq_i = r % p.sq;
                             const int qrow = (sg.b * p.sq + sq_i) * p.H + sg.g * p.heads_per_group + j;
                             const uint4* src = reinterpret_cast<const uint4*>(p.q + (size_t)qrow * D) + 2 * c16;
-                            a = __ldg(src);
-                            b = __ldg(src + 1);
+                            qa4[u] = __ldg(src);
+                            qb4[u] = __ldg(src + 1);
                         }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kIters; ++u) {
+                        const int idx = lane + 32 * u;
+                        const int row = idx / (D / 16), c16 = idx % (D / 16);
+                        const uint4 a = qa4[u], b = qb4[u];
                         const uint4 ev = make_uint4(bf16x2_to_f16x2(a.x), bf16x2_to_f16x2(a.z),
                                                     bf16x2_to_f16x2(b.x), bf16x2_to_f16x2(b.z));
                         const uint4 od = make_uint4(bf16x2_to_f16x2(a.y), bf16x2_to_f16x2(a.w),
@@ -583,16 +633,25 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                         *reinterpret_cast<uint4*>(qw + row * (D * 2) + (((2 * c16 + 1) ^ (row & 7)) << 4)) = od;
                     }
                 } else {
-                    for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
+                    constexpr int kIters = 16 * (D / 8) / 32;
+                    uint4 v[kIters];
+#pragma unroll
+                    for (int u = 0; u < kIters; ++u) {
+                        const int idx = lane + 32 * u;
                         const int row = idx / (D / 8), chunk = idx % (D / 8);
                         const int r = mt * 16 + row;
-                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        v[u] = make_uint4(0u, 0u, 0u, 0u);
                         if (r < p.R) {
                             const int j = r / p.sq, sq_i = r % p.sq;
                             const int qrow = (sg.b * p.sq + sq_i) * p.H + sg.g * p.heads_per_group + j;
-                            v = __ldg(reinterpret_cast<const uint4*>(p.q + (size_t)qrow * D) + chunk);
+                            v[u] = __ldg(reinterpret_cast<const uint4*>(p.q + (size_t)qrow * D) + chunk);
                         }
-                        *reinterpret_cast<uint4*>(qw + row * (D * 2) + ((chunk ^ (row & 7)) << 4)) = v;
+                    }
+#pragma unroll
+                    for (int u = 0; u < kIters; ++u) {
+                        const int idx = lane + 32 * u;
+                        const int row = idx / (D / 8), chunk = idx % (D / 8);
+                        *reinterpret_cast<uint4*>(qw + row * (D * 2) + ((chunk ^ (row & 7)) << 4)) = v[u];
                     }
                 }
                 __syncwarp();
@@ -645,8 +704,8 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             if (tbase + kTileTokens > sg.tb) {
                 constexpr int kChunks = D * KS::kElemBytes / 16;   // 16-byte chunks per row
                 bool wrote = false;
-                for (int idx = lane; idx < 16 * kChunks; idx += 32) {
-                    const int row = slice * 16 + idx / kChunks;
+                for (int idx = lane; idx < WT * kChunks; idx += 32) {
+                    const int row = tok0 + idx / kChunks;
                     const int chunk = idx % kChunks;
                     if (tbase + row >= sg.tb) {
                         const int bx = chunk >> 3, cc = chunk & 7;
@@ -658,15 +717,15 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                 __syncwarp();
             }
 
-            // Fused append: the new tokens' rows of this warp's 16-token slice
+            // Fused append: the new tokens' rows of this warp's slice
             // come from k_new/v_new, not from the cache the TMA just read. The
             // warp patches them into the stage before reading it and (one row
             // tile's warp) stores them to the cache. Each position lies in
             // exactly one tile, which one CTA owns, so no other CTA reads it.
             if (!KV8 && p.k_new != nullptr) {
                 const int new_lo = sg.tb - p.sq;
-                const int lo = max(new_lo, tbase + slice * 16);
-                const int hi = min(sg.tb, tbase + slice * 16 + 16);
+                const int lo = max(new_lo, tbase + tok0);
+                const int hi = min(sg.tb, tbase + tok0 + WT);
                 if (lo < hi) {
                     const size_t unit_row0 = ((size_t)sg.b * p.G + sg.g) * p.Tmax;
                     for (int idx = lane; idx < (hi - lo) * (D / 8); idx += 32) {
@@ -690,8 +749,10 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                 }
             }
 
-            // S = Q K^T for this warp's 16 tokens: two n8 tiles.
-            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            // S = Q K^T for this warp's tokens: NJ n8 tiles.
+            float sc[NJ][4];
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
             if constexpr (KV8) {
                 // e4m3 codes straight from the stage: an 8x8 b16 ldmatrix of K
                 // rows gives each thread 4 consecutive codes (d = 4q..4q+3 of a
@@ -728,55 +789,46 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                         for (int c = 0; c < 4; ++c) sc[j][c] += sd[j][c];
                 }
             } else {
-                // Two row tiles: odd k steps accumulate apart from even ones
-                // (summed after the loop), which halves the dependent MMA chains
-                // that bound these warps.
-                constexpr bool kSplitK = MT > 1;
-                float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                // Each k step: one Q fragment, NJ/2 ldmatrix of K (16 tokens
+                // each), NJ independent MMA chains.
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; ++kk) {
                     const int chunk = kk * 2 + k_half;
                     const int bx = chunk >> 3, cc = chunk & 7;
-                    uint32_t b0, b1, b2, b3;
-                    if constexpr (KS::kPageMajor)
-                        ldsm_x4(kst + k_off0 + bx * bx_stride + ((cc ^ (k_tok & 7)) << 4), b0, b1, b2, b3);
-                    else
-                        ldsm_x4(kst + bx * (kTileTokens * 128) + k_tok * 128 + ((cc ^ (k_tok & 7)) << 4), b0, b1,
-                                b2, b3);
                     uint32_t a_s[4];
                     if constexpr (kQs) {
                         const int qc = kk * 2 + (lane >> 4);
                         ldsm_x4(qa_base + ((qc ^ (qa_row & 7)) << 4), a_s[0], a_s[1], a_s[2], a_s[3]);
                     }
                     const uint32_t(&a)[4] = kQs ? a_s : qa[kQs ? 0 : kk];
-                    if (kSplitK && (kk & 1)) {
-                        mma_bf16_16816(sd[0], a, b0, b1);
-                        mma_bf16_16816(sd[1], a, b2, b3);
-                    } else {
-                        mma_bf16_16816(sc[0], a, b0, b1);
-                        mma_bf16_16816(sc[1], a, b2, b3);
+#pragma unroll
+                    for (int jj = 0; jj < NJ / 2; ++jj) {
+                        // (k_tok + 16 jj) & 7 == k_tok & 7: the same swizzle.
+                        uint32_t b0, b1, b2, b3;
+                        if constexpr (KS::kPageMajor)
+                            ldsm_x4(kst + k_off0[jj] + bx * bx_stride + ((cc ^ (k_tok & 7)) << 4), b0, b1, b2, b3);
+                        else
+                            ldsm_x4(kst + bx * (kTileTokens * 128) + (k_tok + 16 * jj) * 128 +
+                                        ((cc ^ (k_tok & 7)) << 4),
+                                    b0, b1, b2, b3);
+                        mma_bf16_16816(sc[2 * jj], a, b0, b1);
+                        mma_bf16_16816(sc[2 * jj + 1], a, b2, b3);
                     }
-                }
-                if constexpr (kSplitK) {
-#pragma unroll
-                    for (int j = 0; j < 2; ++j)
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) sc[j][c] += sd[j][c];
                 }
             }
             const float sscale = KV8 ? p.scale_log2 * ks : p.scale_log2;
 
             // Scale into the base-2 domain and mask invisible keys.
-            float x[2][4];
+            float x[NJ][4];
             if (tbase + kTileTokens - 1 <= lim_min) {
 #pragma unroll
-                for (int j = 0; j < 2; ++j)
+                for (int j = 0; j < NJ; ++j)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) x[j][c] = sc[j][c] * sscale;
             } else {
-                const int tok = tbase + slice * 16 + 2 * quad;
+                const int tok = tbase + tok0 + 2 * quad;
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
+                for (int j = 0; j < NJ; ++j) {
                     const int t = tok + 8 * j;
                     x[j][0] = (t <= lim_lo) ? sc[j][0] * sscale : -INFINITY;
                     x[j][1] = (t + 1 <= lim_lo) ? sc[j][1] * sscale : -INFINITY;
@@ -786,6 +838,11 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             }
             float mx_lo = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
             float mx_hi = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+#pragma unroll
+            for (int j = 2; j < NJ; j += 2) {
+                mx_lo = fmaxf(mx_lo, fmaxf(fmaxf(x[j][0], x[j][1]), fmaxf(x[j + 1][0], x[j + 1][1])));
+                mx_hi = fmaxf(mx_hi, fmaxf(fmaxf(x[j][2], x[j][3]), fmaxf(x[j + 1][2], x[j + 1][3])));
+            }
             mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
             mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
             mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
@@ -801,9 +858,9 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             const float base_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
             const float base_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
 
-            float pr[2][4];
+            float pr[NJ][4];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
+            for (int j = 0; j < NJ; ++j) {
                 pr[j][0] = fast_exp2(x[j][0] - base_lo);
                 pr[j][1] = fast_exp2(x[j][1] - base_lo);
                 pr[j][2] = fast_exp2(x[j][2] - base_hi);
@@ -823,22 +880,29 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             }
             m_lo = mn_lo;
             m_hi = mn_hi;
-            l_lo += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-            l_hi += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+#pragma unroll
+            for (int j = 0; j < NJ; j += 2) {
+                l_lo += (pr[j][0] + pr[j][1]) + (pr[j + 1][0] + pr[j + 1][1]);
+                l_hi += (pr[j][2] + pr[j][3]) + (pr[j + 1][2] + pr[j + 1][3]);
+            }
 
-            // The S accumulator layout is the A-operand layout of P.V.
-            uint32_t pa[4];
-            if constexpr (KV8) {
-                // P times the tile's V scale: O accumulates code-valued V.
-                pa[0] = pack_f16x2(pr[0][0] * vs, pr[0][1] * vs);
-                pa[1] = pack_f16x2(pr[0][2] * vs, pr[0][3] * vs);
-                pa[2] = pack_f16x2(pr[1][0] * vs, pr[1][1] * vs);
-                pa[3] = pack_f16x2(pr[1][2] * vs, pr[1][3] * vs);
-            } else {
-                pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
-                pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
-                pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
-                pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+            // The S accumulator layout is the A-operand layout of P.V: n8
+            // token tiles 2kk and 2kk + 1 are the A fragment of k step kk.
+            uint32_t pa[NJ / 2][4];
+#pragma unroll
+            for (int kk = 0; kk < NJ / 2; ++kk) {
+                if constexpr (KV8) {
+                    // P times the tile's V scale: O accumulates code-valued V.
+                    pa[kk][0] = pack_f16x2(pr[2 * kk][0] * vs, pr[2 * kk][1] * vs);
+                    pa[kk][1] = pack_f16x2(pr[2 * kk][2] * vs, pr[2 * kk][3] * vs);
+                    pa[kk][2] = pack_f16x2(pr[2 * kk + 1][0] * vs, pr[2 * kk + 1][1] * vs);
+                    pa[kk][3] = pack_f16x2(pr[2 * kk + 1][2] * vs, pr[2 * kk + 1][3] * vs);
+                } else {
+                    pa[kk][0] = pack_bf16x2(pr[2 * kk][0], pr[2 * kk][1]);
+                    pa[kk][1] = pack_bf16x2(pr[2 * kk][2], pr[2 * kk][3]);
+                    pa[kk][2] = pack_bf16x2(pr[2 * kk + 1][0], pr[2 * kk + 1][1]);
+                    pa[kk][3] = pack_bf16x2(pr[2 * kk + 1][2], pr[2 * kk + 1][3]);
+                }
             }
             if constexpr (KV8) {
                 // e4m3 V: a transposed 8x8 b16 ldmatrix of V rows gives each
@@ -855,27 +919,32 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const uint32_t lo = r[2 * e], hi = r[2 * e + 1];   // tokens 0-7, 8-15
-                        mma_f16_16816(o[2 * (blk + e)], pa,
+                        mma_f16_16816(o[2 * (blk + e)], pa[0],
                                       e4m3x2_to_f16x2((uint16_t)__byte_perm(lo, 0u, 0x0020)),
                                       e4m3x2_to_f16x2((uint16_t)__byte_perm(hi, 0u, 0x0020)));
-                        mma_f16_16816(o[2 * (blk + e) + 1], pa,
+                        mma_f16_16816(o[2 * (blk + e) + 1], pa[0],
                                       e4m3x2_to_f16x2((uint16_t)__byte_perm(lo, 0u, 0x0031)),
                                       e4m3x2_to_f16x2((uint16_t)__byte_perm(hi, 0u, 0x0031)));
                     }
                 }
             } else {
 #pragma unroll
-                for (int n = 0; n < NTILE_D; n += 2) {
-                    const int chunk = n + v_dt;
-                    const int bx = chunk >> 3, cc = chunk & 7;
-                    uint32_t b0, b1, b2, b3;
-                    if constexpr (KS::kPageMajor)
-                        ldsm_x4_trans(vst + v_off0 + bx * bx_stride + ((cc ^ (v_tok & 7)) << 4), b0, b1, b2, b3);
-                    else
-                        ldsm_x4_trans(vst + bx * (kTileTokens * 128) + v_tok * 128 + ((cc ^ (v_tok & 7)) << 4), b0,
-                                      b1, b2, b3);
-                    mma_bf16_16816(o[n], pa, b0, b1);
-                    mma_bf16_16816(o[n + 1], pa, b2, b3);
+                for (int kk = 0; kk < NJ / 2; ++kk) {
+#pragma unroll
+                    for (int n = 0; n < NTILE_D; n += 2) {
+                        const int chunk = n + v_dt;
+                        const int bx = chunk >> 3, cc = chunk & 7;
+                        uint32_t b0, b1, b2, b3;
+                        if constexpr (KS::kPageMajor)
+                            ldsm_x4_trans(vst + v_off0[kk] + bx * bx_stride + ((cc ^ (v_tok & 7)) << 4), b0, b1, b2,
+                                          b3);
+                        else
+                            ldsm_x4_trans(vst + bx * (kTileTokens * 128) + (v_tok + 16 * kk) * 128 +
+                                              ((cc ^ (v_tok & 7)) << 4),
+                                          b0, b1, b2, b3);
+                        mma_bf16_16816(o[n], pa[kk], b0, b1);
+                        mma_bf16_16816(o[n + 1], pa[kk], b2, b3);
+                    }
                 }
             }
             __syncwarp();
@@ -1078,18 +1147,8 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             __threadfence();
             __syncwarp();
             if (lane == 0) {
-                // With at least one tile per CTA every CTA from cf to cl has
-                // a share of the unit; otherwise count the non-empty ones.
-                unsigned contributors = (unsigned)(cl - cf + 1);
-                if (W < P) {
-                    contributors = 0;
-                    for (long long c = cf; c <= cl; ++c)
-                        contributors += (c * W / P) < ((c + 1) * W / P) ? 1u : 0u;
-                }
-                unsigned long long* ctr = p.ws_counters + ((size_t)sg.b * p.G + sg.g) * kMaxRowTiles + mt;
-                const unsigned arrived = arrive_unit(ctr, p.epoch, p.status);
-                last_flag[mt] = arrived == contributors ? 1 : 0;
-                if (arrived == contributors) release_unit(ctr);
+                last_flag[mt] = arrive_and_release(p, sg, mt, W, P) ? 1 : 0;
+                arrived_here = true;
             }
         }
         mbar_arrive(mbarC);
@@ -1247,7 +1306,26 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
         }
     }
 
-    if (failed) return;  // a wait gave up; the status word says so
+    if (failed) {
+        // A wait gave up; the status word says so and the outputs are
+        // undefined. The counters must still end the launch at zero: a CUDA
+        // graph replays this launch with the same epoch, and a count left
+        // part-way would let the next replay merge before its partials are
+        // written. So the row tile's slice-0 lane 0 counts this CTA's arrival
+        // on every partial unit of its share it has not counted yet (the
+        // interrupted segment included); the arrival that completes a count
+        // resets the counter as usual, and no merge runs here.
+        if (slice == 0 && group == 0 && lane == 0) {
+            bool have = true;
+            bool counted = arrived_here;
+            while (have) {
+                if (!sg.complete && !counted) arrive_and_release(p, sg, mt, W, P);
+                counted = false;
+                have = walk.next(sg);
+            }
+        }
+        return;
+    }
 
     // ---- sequences with no valid entry have no tile and no CTA: CTA
     // (b mod grid) writes out = 0 and lse = -inf for all their rows.

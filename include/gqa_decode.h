@@ -247,7 +247,11 @@ int gqa_decode_check_error(cudaStream_t stream);
  * implicit synchronisation. The pages have no counterpart of this; it is a
  * property of this library's interface, not of the attention it computes.
  *
- * Same arguments, layouts and results as gqa_decode. The split-KV scratch
+ * Same arguments, layouts and results as gqa_decode for up to 32 query rows
+ * per KV head, (H/G)*sq <= 32: the split-KV decode kernel. gqa_decode sends
+ * larger row counts to the prefill kernel, whose split key ranges take a
+ * library-allocated workspace, so this entry point refuses them with
+ * GQA_ERR_UNSUPPORTED and enqueues nothing. The split-KV scratch
  * comes from a fixed array of GQA_NOALLOC_SCRATCH_BYTES in device memory that
  * every GPU which loads the library holds until the process exits; the call
  * makes no cudaMalloc or cudaFree. The first call on a device looks up that
@@ -266,6 +270,20 @@ int gqa_decode_check_error(cudaStream_t stream);
 int gqa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* seq_lens, float scale, void* out, float* lse,
                        int B, int sq, int H, int G, int D, int Tmax, cudaStream_t stream);
+
+/*
+ * Frees the workspace the library owns for (current device, `stream`), the
+ * one gqa_decode, gqa_decode_append, gqa_decode_paged, gqa_decode_fp8 and
+ * gqa_prefill grow on that stream. Call it before destroying a stream that
+ * the library was used on, or to give the memory back; a later call on the
+ * stream allocates again. It synchronises `stream` first (work already
+ * queued may use the buffer). Returns GQA_OK (also when the library holds
+ * nothing for the stream) or GQA_ERR_CUDA. The pages have no counterpart of
+ * this; it belongs to this library's memory management ("GQA analysis",
+ * section "Incremental decode", leaves the cache to the caller, so the
+ * library's own buffers are the only memory it has to give back).
+ */
+int gqa_decode_release_workspace(cudaStream_t stream);
 
 /* The cudaError_t of the last failed CUDA call in this thread (0 if none). */
 int gqa_decode_last_cuda_error(void);

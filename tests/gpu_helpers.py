@@ -87,15 +87,6 @@ def env(**kv):
                 os.environ[k] = v
 
 
-def split_kv_kernel():
-    """Contiguous decode on the m16n8k16 split-KV kernel for every row count
-    (the default; GQA_DECODE_TC=1 in the caller's environment would send
-    17..32 rows to the tcgen05 kernel): the paged, fp8 and fused-append paths
-    run on that kernel, so their bit-for-bit comparisons with the contiguous
-    path are made against it."""
-    return env(GQA_DECODE_TC="0")
-
-
 def run_gpu(q, k, v, lens, scale, with_lse=True, device_inputs=None, entry=None):
     """Runs gqa_decode (or `entry`, a binding with its signature) on the device. Returns (out float64 [B,sq,H,D], lse
     float64 [B,sq,H] or None). Checks that the guard words around out and lse

@@ -38,9 +38,9 @@ def _lens(rng, B, Tmax, sq):
     return rng.integers(sq, Tmax + 1, size=B).astype(np.int32)
 
 
-@pytest.mark.parametrize("H,G,sq,tc", [(32, 8, 1, "0"), (64, 8, 4, "0"), (32, 1, 1, "1")],
-                         ids=["one-row-tile", "two-row-tiles", "tcgen05-opt-in"])
-def test_decode_graph_replays(H, G, sq, tc):
+@pytest.mark.parametrize("H,G,sq", [(32, 8, 1), (64, 8, 4), (32, 1, 1)],
+                         ids=["one-row-tile", "two-row-tiles", "mqa-two-row-tiles"])
+def test_decode_graph_replays(H, G, sq):
     B, D, Tmax = 3, 128, 1500
     rng = np.random.default_rng(1701 + H + sq)
     scale = 1 / math.sqrt(D)
@@ -59,7 +59,7 @@ def test_decode_graph_replays(H, G, sq, tc):
 
     load(1800)
     s = torch.cuda.Stream()
-    with min_tiles(1), env(GQA_DECODE_TC=tc):
+    with min_tiles(1):
         g = _graph(lambda: gq.gqa_decode(dq, dk, dv, dl, scale, out, lse), s)
     for rep in range(REPLAYS):
         q, k, v, lens = load(1801 + rep)
@@ -69,7 +69,7 @@ def test_decode_graph_replays(H, G, sq, tc):
         assert gq.gqa_decode_check_error() == gq.GQA_OK
         ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, scale, threads=8)
         compare(bf16_to_f64(out), lse.cpu().numpy().astype(np.float64), ref_out, ref_lse,
-                what=f"graph replay {rep} H={H} sq={sq} tc={tc}")
+                what=f"graph replay {rep} H={H} sq={sq}")
 
 
 def test_variant_graph_replays():

@@ -9,7 +9,7 @@ import torch
 import grouped_query_decode_gb300 as gq
 import oracle
 import synthetic as syn
-from gpu_helpers import bf16_to_f64, compare, make_inputs, min_tiles, run_gpu, split_kv_kernel, to_device_bf16
+from gpu_helpers import bf16_to_f64, compare, make_inputs, min_tiles, run_gpu, to_device_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -36,7 +36,7 @@ def test_paged_matches_oracle_and_contiguous(H, G, sq, D, page_size, split):
     kp, vp, table = syn.paginate(k, v, lens, page_size, seed=701 + page_size)
     scale = 1 / math.sqrt(D)
     ref_out, ref_lse = oracle.gqa_decode_paged_f64(q, kp, vp, table, lens, scale, threads=8)
-    with min_tiles(split), split_kv_kernel():
+    with min_tiles(split):
         out, lse = _run_paged(q, kp, vp, table, lens, scale)
         cont_out, cont_lse = run_gpu(q, k, v, lens, scale)
     compare(out, lse, ref_out, ref_lse, what=f"paged ps={page_size}")

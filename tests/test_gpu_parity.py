@@ -13,7 +13,7 @@ import torch
 import grouped_query_decode_gb300 as gq
 import oracle
 import synthetic as syn
-from gpu_helpers import compare, make_inputs, min_tiles, run_gpu, to_device_bf16
+from gpu_helpers import bf16_to_f64, compare, make_inputs, min_tiles, run_gpu, to_device_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -152,6 +152,60 @@ def test_explicit_workspace_matches_library_workspace():
         assert e.value.status == gq.GQA_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+
+
+def test_explicit_workspace_guard_words():
+    """Canary bytes on both sides of a caller-owned workspace stay untouched by
+    a call whose plan splits units over many CTAs (every CTA writes partial
+    slots, the counters are used), and the result matches the oracle."""
+    B, sq, H, G, D, Tmax = 3, 4, 64, 8, 128, 900
+    q, k, v, lens = make_inputs(B, sq, H, G, D, Tmax, [900, 517, 77], seed=208)
+    dq, dk, dv = to_device_bf16(q), to_device_bf16(k), to_device_bf16(v)
+    dl = torch.from_numpy(lens).cuda()
+    out = torch.empty(B, sq, H, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, sq, H, dtype=torch.float32, device="cuda")
+    guard = 4096
+    with min_tiles(1):
+        nbytes = gq.gqa_decode_workspace_bytes(B, sq, H, G, D, Tmax)
+        buf = torch.full((nbytes + 2 * guard,), 0xA5, dtype=torch.uint8, device="cuda")
+        ws = buf[guard:guard + nbytes]
+        assert ws.data_ptr() % 256 == 0
+        for _ in range(2):
+            gq.gqa_decode_ex(dq, dk, dv, dl, 1 / math.sqrt(D), out, lse, ws)
+    torch.cuda.synchronize()
+    assert gq.gqa_decode_check_error() == gq.GQA_OK
+    host = buf.cpu().numpy()
+    assert np.all(host[:guard] == 0xA5) and np.all(host[guard + nbytes:] == 0xA5), "workspace guard"
+    ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, 1 / math.sqrt(D), threads=8)
+    compare(bf16_to_f64(out), lse.cpu().numpy().astype(np.float64), ref_out, ref_lse, what="guarded workspace")
+
+
+def test_release_workspace_frees_and_the_next_call_allocates_again():
+    """gqa_decode_release_workspace gives the (device, stream) buffer back:
+    the device's free memory grows by about its size, and the next call on
+    the stream allocates a new one and is still correct."""
+    B, sq, H, G, D, Tmax = 64, 1, 32, 1, 128, 2048
+    q, k, v, lens = make_inputs(B, sq, H, G, D, Tmax, [2048] * B, seed=209)
+    dq, dk, dv = to_device_bf16(q), to_device_bf16(k), to_device_bf16(v)
+    dl = torch.from_numpy(lens).cuda()
+    out = torch.empty(B, sq, H, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, sq, H, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    need = gq.gqa_decode_workspace_bytes(B, sq, H, G, D, Tmax)
+    assert need > 2 << 20
+    gq.gqa_decode(dq, dk, dv, dl, 1 / math.sqrt(D), out, lse, stream=s)
+    s.synchronize()
+    free_held, _ = torch.cuda.mem_get_info()
+    gq.gqa_decode_release_workspace(s)
+    free_released, _ = torch.cuda.mem_get_info()
+    assert free_released - free_held >= need // 2, (free_held, free_released, need)
+    gq.gqa_decode_release_workspace(s)          # nothing held: still fine
+    ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, 1 / math.sqrt(D), threads=8)
+    gq.gqa_decode(dq, dk, dv, dl, 1 / math.sqrt(D), out, lse, stream=s)
+    s.synchronize()
+    assert gq.gqa_decode_check_error(s) == gq.GQA_OK
+    compare(bf16_to_f64(out), lse.cpu().numpy().astype(np.float64), ref_out, ref_lse, what="after release")
+    gq.gqa_decode_release_workspace(s)
 
 
 def test_repeated_calls_are_bit_identical():

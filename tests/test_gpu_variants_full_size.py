@@ -10,7 +10,7 @@ import torch
 import grouped_query_decode_gb300 as gq
 import oracle
 import synthetic as syn
-from gpu_helpers import bf16_to_f64, compare, run_gpu, split_kv_kernel, to_device_bf16
+from gpu_helpers import bf16_to_f64, compare, run_gpu, to_device_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -56,8 +56,7 @@ def test_paged_full_size_equals_contiguous(name, page_size):
     cfg = syn.config_by_name(name)
     q, k, v, lens = syn.make_inputs(cfg, threads=16)
     kp, vp, table = syn.paginate(k, v, lens, page_size, seed=cfg.seed + 100)
-    with split_kv_kernel():
-        cont_out, cont_lse = run_gpu(q, k, v, lens, cfg.scale)
+    cont_out, cont_lse = run_gpu(q, k, v, lens, cfg.scale)
     out = torch.empty(cfg.B, cfg.sq, cfg.H, cfg.D, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(cfg.B, cfg.sq, cfg.H, dtype=torch.float32, device="cuda")
     gq.gqa_decode_paged(to_device_bf16(q), to_device_bf16(kp), to_device_bf16(vp),
@@ -83,7 +82,6 @@ def test_append_full_size_equals_write_then_decode():
     k2, v2 = oracle.append_f64(k, v, kn, vn, lens)       # the rows written where the pages say
     assert np.array_equal(dk.cpu().view(torch.int16).numpy().view(np.uint16), k2)
     assert np.array_equal(dv.cpu().view(torch.int16).numpy().view(np.uint16), v2)
-    with split_kv_kernel():
-        ref_out, ref_lse = run_gpu(q, k2, v2, lens, cfg.scale)
+    ref_out, ref_lse = run_gpu(q, k2, v2, lens, cfg.scale)
     assert np.array_equal(bf16_to_f64(out), ref_out)
     assert np.array_equal(lse.cpu().numpy().astype(np.float64), ref_lse)

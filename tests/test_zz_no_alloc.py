@@ -57,8 +57,9 @@ def test_noalloc_matches_regular_entry_point(shape, split):
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch():
-    # 2^21 one-token sequences need 16 MiB of per-sequence tile offsets alone,
-    # more than the fixed array holds; the call must be refused up front.
+    # 2^21 one-token sequences need 32 MiB of arrival counters alone (8 B per
+    # sequence, KV head and row tile), more than the fixed array holds; the
+    # call must be refused up front.
     B = 1 << 21
     need = gq.gqa_decode_workspace_bytes(B, 1, 1, 1, 64, 64)
     assert need > gq.GQA_NOALLOC_SCRATCH_BYTES
@@ -68,5 +69,20 @@ def test_noalloc_refuses_problems_beyond_its_scratch():
     rc = gq.load().gqa_decode_noalloc(p, p, p, lens.data_ptr(), 0.125, p, None,
                                       B, 1, 1, 1, 64, 64, None)
     assert rc == gq.GQA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert gq.gqa_decode_check_error() == gq.GQA_OK
+
+
+def test_noalloc_refuses_more_than_32_rows_per_kv_head():
+    # gqa_decode sends (H/G)*sq > 32 rows to the prefill kernel, whose split
+    # key ranges use a library-allocated workspace; the allocation-free entry
+    # point does not, and refuses such shapes before anything is enqueued.
+    B, sq, H, G, D, Tmax = 1, 1, 64, 1, 128, 256
+    dq = torch.zeros(B, sq, H, D, dtype=torch.bfloat16, device="cuda")
+    dk = torch.zeros(B, G, Tmax, D, dtype=torch.bfloat16, device="cuda")
+    dl = torch.full((B,), Tmax, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, sq, H, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, sq, H, dtype=torch.float32, device="cuda")
+    assert _abi_noalloc(dq, dk, dk, dl, D ** -0.5, out, lse) == gq.GQA_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert gq.gqa_decode_check_error() == gq.GQA_OK
