@@ -286,6 +286,7 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32
     a.p.heads_per_group = H / G;
     a.p.ctas = plan.ctas;
     a.p.even_rule = forced_ctas() > 0 ? 0 : 1;
+    a.p.small_plan = (B <= 64 && plan.max_tiles < (1ll << 31)) ? 1 : 0;
     debug_knobs(&a.p.wait_timeout_ns, &a.p.skip_tile);
     a.p.k_new = static_cast<const uint16_t*>(k_new);
     a.p.v_new = static_cast<const uint16_t*>(v_new);

@@ -54,6 +54,7 @@ struct DecodeParams {
     float scale_log2;        // scale * log2(e)
     int B, sq, H, G, Tmax, R, heads_per_group, ctas;
     int even_rule;           // 1: use fewer CTAs when that splits no unit (see kernel)
+    int small_plan;          // 1: B <= 64 and B * G * ceil(Tmax / 64) < 2^31 (32-bit plan)
     int skip_tile;           // fault injection for tests: CTA 0 never loads its tile
                              // number skip_tile (-1: off), so its consumers' wait expires
     // Fused append (all null for a plain decode): the sq new tokens' K/V,
@@ -152,7 +153,7 @@ struct KernelShape {
     static constexpr int kMlBytes = MT * kSlices * 16 * 2 * 4;
     static constexpr int kQBytes = kConsumerWarps * kQBytesPerWarp;
     // fp8 stages are half as large: twice as many keep the same bytes in flight.
-    static constexpr int kStages = KV8 ? 8 : (D == 128 ? (MT == 1 ? 6 : 4) : 8);
+    static constexpr int kStages = KV8 ? 8 : (D == 128 ? 4 : 8);
     // With groups on alternate tiles, a warp waits on tile t having read only
     // every other tile before it. Tile t - kStages, the stage's previous
     // load, must then be its own group's (read, hence landed, by this warp):

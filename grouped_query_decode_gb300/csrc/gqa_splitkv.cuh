@@ -40,6 +40,12 @@ struct Segment {
     bool first;          // the CTA's first segment (partial slot 0, else slot 1)
 };
 
+// A compile-time int carried by a value (template arguments of generic lambdas).
+template <int N>
+struct IntC {
+    static constexpr int value = N;
+};
+
 // Tiles of TT tokens covering tb valid tokens.
 template <int TT = kTileTokens>
 __device__ __forceinline__ long long tiles_of(int tb) { return (tb + TT - 1) / TT; }
@@ -65,7 +71,9 @@ struct SegmentWalkerT {
                 continue;
             }
             const long long off = x - pre_b;
-            const int g = (int)(off / nt);
+            // 32-bit division when both fit (every workload here): a far
+            // shorter instruction sequence than the 64-bit one.
+            const int g = (off < (1ll << 31) && nt < (1ll << 31)) ? (int)off / (int)nt : (int)(off / nt);
             const long long ub = pre_b + (long long)g * nt, ue = ub + nt;
             const long long e = hi < ue ? hi : ue;
             s.b = b;
@@ -326,6 +334,67 @@ struct TileIssuer {
 // whole number of CTAs per unit (every CTA one equal partial) on about 85%
 // of the grid (kSplitEven; a kernel whose merges are cheap keeps every CTA).
 // The CTAs left over exit.
+// plan_share for up to 64 sequences and fewer than 2^31 tiles in all
+// (DecodeParams::small_plan, set by the host from B and B * G *
+// ceil(Tmax / 64)): lane i holds sequences i and i + 32, and every sum is a
+// 32-bit scan. Same result as plan_share; it exists because every kernel
+// launch pays for the plan before its first copy, in instruction fetches
+// of cold code more than in arithmetic, so the plan is kept short.
+template <int TT>
+__device__ __forceinline__ void plan_share_small(const DecodeParams& p, int lane, long long* shared_ll) {
+    const bool has0 = lane < p.B, has1 = lane + 32 < p.B;
+    const int n0 = has0 ? (int)tiles_of<TT>(clamp_len(__ldg(p.seq_lens + lane), p.Tmax)) : 0;
+    const int n1 = has1 ? (int)tiles_of<TT>(clamp_len(__ldg(p.seq_lens + lane + 32), p.Tmax)) : 0;
+    const int v0 = n0 * p.G, v1 = n1 * p.G;
+    int s0 = v0, s1 = v1;   // inclusive scans over the lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u0 = __shfl_up_sync(0xffffffffu, s0, o), u1 = __shfl_up_sync(0xffffffffu, s1, o);
+        if (lane >= o) {
+            s0 += u0;
+            s1 += u1;
+        }
+    }
+    const int tot0 = __shfl_sync(0xffffffffu, s0, 31);
+    const int total = tot0 + __shfl_sync(0xffffffffu, s1, 31);
+    const unsigned big = 0x7fffffffu;
+    const int nt_min = (int)__reduce_min_sync(0xffffffffu, min(has0 ? (unsigned)n0 : big, has1 ? (unsigned)n1 : big));
+    const int nt_max = (int)__reduce_max_sync(0xffffffffu, (unsigned)max(n0, n1));
+    int P = p.ctas;
+    if (p.even_rule && nt_min == nt_max && nt_max > 0) {
+        const int units = p.B * p.G;
+        if (units >= P) {
+            const int per = (units + P - 1) / P;
+            const int even = (units + per - 1) / per;
+            if (units % per == 0 && 5 * even >= 4 * P) P = even;
+        } else {
+            const int even = units * ((P * 85 / 100) / units);
+            if (even >= units && 5 * even >= 4 * P) P = even;
+        }
+    }
+    int bstart = p.B, prestart = total;
+    if ((int)blockIdx.x < P) {
+        const int lo = (int)(((long long)blockIdx.x * total) / P);
+        const unsigned hit0 = __ballot_sync(0xffffffffu, has0 && s0 > lo);
+        const unsigned hit1 = __ballot_sync(0xffffffffu, has1 && tot0 + s1 > lo);
+        if (hit0) {
+            const int src = __ffs(hit0) - 1;
+            bstart = src;
+            prestart = __shfl_sync(0xffffffffu, s0 - v0, src);
+        } else if (hit1) {
+            const int src = __ffs(hit1) - 1;
+            bstart = 32 + src;
+            prestart = tot0 + __shfl_sync(0xffffffffu, s1 - v1, src);
+        }
+    }
+    if (lane == 0) {
+        shared_ll[0] = total;
+        shared_ll[1] = bstart;
+        shared_ll[2] = prestart;
+        shared_ll[3] = P;
+    }
+}
+
 template <int TT, bool kSplitEven = true>
 __device__ __forceinline__ void plan_share(const DecodeParams& p, int lane, long long* shared_ll) {
     constexpr int kCached = 8;       // sequences 0..255 stay in registers
@@ -459,7 +528,12 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     pdl_wait_primary();
 
     // Warp 0: this CTA's share of the tiles (plan_share).
-    if (warp == 0) plan_share<kTileTokens>(p, lane, shared_ll);
+    if (warp == 0) {
+        if (p.small_plan)
+            plan_share_small<kTileTokens>(p, lane, shared_ll);
+        else
+            plan_share<kTileTokens>(p, lane, shared_ll);
+    }
     __syncthreads();
     pdl_launch_dependents();
 
@@ -1166,47 +1240,69 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             const int ncand = (int)(cl - cf + 1);
             const int first_slot = (int)(cf * 2 + ((cf * W / P) == sg.ub ? 0 : 1));
             const int rows_here = (p.R - mt * 16) < 16 ? (p.R - mt * 16) : 16;
-            constexpr int C4 = D / 4;
-            for (int item = tid_mt; item < rows_here * C4; item += kSlices * 32) {
-                const int rr = item / C4;
-                const int r = mt * 16 + rr;
-                const int c4 = (item % C4) * 4;
-                float mk[KS::kFastMerge], lk[KS::kFastMerge];
-                float4 ok4[KS::kFastMerge];
+            // NC candidate slots held per item, NI items of this thread merged
+            // from one round of loads (up to four with at most two
+            // contributors, the common split of a unit over two CTAs).
+            auto merge_items = [&](auto nc_c, auto ni_c) {
+                constexpr int NC = decltype(nc_c)::value, NI = decltype(ni_c)::value;
+                constexpr int C4 = D / 4;
+                const int n_items = rows_here * C4;
+                for (int item0 = tid_mt; item0 < n_items; item0 += NI * kSlices * 32) {
+                    float mk[NI][NC], lk[NI][NC];
+                    float4 ok4[NI][NC];
 #pragma unroll
-                for (int k = 0; k < KS::kFastMerge; ++k) {
-                    mk[k] = -INFINITY;
-                    lk[k] = 0.f;
-                    ok4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (k < ncand) {
-                        const int sl = k == 0 ? first_slot : (int)((cf + k) * 2);
-                        const float* base = p.ws_part + (size_t)sl * slot_floats;
-                        mk[k] = __ldcg(base + (size_t)p.R * D + r);
-                        lk[k] = __ldcg(base + (size_t)p.R * D + p.R + r);
-                        ok4[k] = __ldcg(reinterpret_cast<const float4*>(base + (size_t)r * D + c4));
+                    for (int u = 0; u < NI; ++u) {
+                        const int item = item0 + u * kSlices * 32;
+                        const int r = mt * 16 + item / C4;
+                        const int c4 = (item % C4) * 4;
+#pragma unroll
+                        for (int k = 0; k < NC; ++k) {
+                            mk[u][k] = -INFINITY;
+                            lk[u][k] = 0.f;
+                            ok4[u][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (k < ncand && item < n_items) {
+                                const int sl = k == 0 ? first_slot : (int)((cf + k) * 2);
+                                const float* base = p.ws_part + (size_t)sl * slot_floats;
+                                mk[u][k] = __ldcg(base + (size_t)p.R * D + r);
+                                lk[u][k] = __ldcg(base + (size_t)p.R * D + p.R + r);
+                                ok4[u][k] = __ldcg(reinterpret_cast<const float4*>(base + (size_t)r * D + c4));
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < NI; ++u) {
+                        const int item = item0 + u * kSlices * 32;
+                        if (item >= n_items) break;
+                        const int r = mt * 16 + item / C4;
+                        const int c4 = (item % C4) * 4;
+                        float M = mk[u][0];
+#pragma unroll
+                        for (int k = 1; k < NC; ++k) M = fmaxf(M, mk[u][k]);
+                        float L = 0.f;
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                        for (int k = 0; k < NC; ++k) {
+                            const float w =
+                                (mk[u][k] == -INFINITY || lk[u][k] == 0.f) ? 0.f : lk[u][k] * fast_exp2(mk[u][k] - M);
+                            L += w;
+                            acc.x += w * ok4[u][k].x;
+                            acc.y += w * ok4[u][k].y;
+                            acc.z += w * ok4[u][k].z;
+                            acc.w += w * ok4[u][k].w;
+                        }
+                        const float inv = L > 0.f ? 1.f / L : 0.f;
+                        const int j = r / p.sq, s = r % p.sq;
+                        const int row = (sg.b * p.sq + s) * p.H + sg.g * p.heads_per_group + j;
+                        *reinterpret_cast<uint2*>(p.out + (size_t)row * D + c4) =
+                            make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+                        if (c4 == 0 && p.lse) p.lse[row] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
                     }
                 }
-                float M = mk[0];
-#pragma unroll
-                for (int k = 1; k < KS::kFastMerge; ++k) M = fmaxf(M, mk[k]);
-                float L = 0.f;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int k = 0; k < KS::kFastMerge; ++k) {
-                    const float w = (mk[k] == -INFINITY || lk[k] == 0.f) ? 0.f : lk[k] * fast_exp2(mk[k] - M);
-                    L += w;
-                    acc.x += w * ok4[k].x;
-                    acc.y += w * ok4[k].y;
-                    acc.z += w * ok4[k].z;
-                    acc.w += w * ok4[k].w;
-                }
-                const float inv = L > 0.f ? 1.f / L : 0.f;
-                const int j = r / p.sq, s = r % p.sq;
-                const int row = (sg.b * p.sq + s) * p.H + sg.g * p.heads_per_group + j;
-                *reinterpret_cast<uint2*>(p.out + (size_t)row * D + c4) =
-                    make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-                if (c4 == 0 && p.lse) p.lse[row] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-            }
+            };
+            if (ncand <= 2)
+                merge_items(IntC<2>{}, IntC<4>{});
+            else
+                merge_items(IntC<KS::kFastMerge>{}, IntC<1>{});
             continue;
         }
 
