@@ -295,6 +295,7 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32
     a.p.block_table = pg.block_table;
     a.p.page_size = pg.page_size;
     a.p.max_pages = pg.max_pages;
+    a.p.page_loader = (pg.block_table && pg.page_size < kTileTokens && !kv8) ? 1 : 0;
     a.p.k_scale = f8.k_scale;
     a.p.v_scale = f8.v_scale;
     a.p.scale_tiles = (Tmax + kTileTokens - 1) / kTileTokens;

@@ -68,6 +68,9 @@ struct DecodeParams {
     // page j of sequence b to its physical page.
     const int32_t* block_table;
     int page_size, max_pages;
+    // Pages shorter than a tile: the two extra warps issue the per-page TMA
+    // boxes (half of a tile's pages each) instead of the producer alone.
+    int page_loader;
     // fp8 caches (KV8 kernels): per (unit, 64-token tile) dequantisation
     // scales, [B*G][scale_tiles] fp32; element value = e4m3 code * scale.
     const float* k_scale;
@@ -118,7 +121,12 @@ struct KernelShape {
     static constexpr int kConsumerWarps = kSlices * MT * (kDual ? 2 : 1);
     // Consumer warps that read each stage (its "empty" barrier's count).
     static constexpr int kStageReaders = kConsumerWarps / kGroups;
-    static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+    // bf16 caches: two more warps issue the TMA boxes of pages shorter than a
+    // tile (DecodeParams::page_loader); they exit at once otherwise. They
+    // cost no registers: the register file is allocated in steps of four
+    // warps (5 -> 8 and 9 -> 12 either way).
+    static constexpr int kLoaderWarps = KV8 ? 0 : 2;
+    static constexpr int kThreads = (kConsumerWarps + 1 + kLoaderWarps) * 32;
     // Registers per thread: the 64K register file for one CTA, with warps
     // counted in the allocation steps of 4, in steps of 8 registers, <= 255.
     static constexpr int kAllocWarps = (kThreads / 32 + 3) / 4 * 4;
