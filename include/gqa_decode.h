@@ -37,10 +37,7 @@
  * KV head, R = (H/G)*sq: up to 32 it runs the split-KV decode kernel, above
  * that the prefill kernel (see gqa_prefill, which also needs scale > 0). The
  * other decode entry points (workspace, plan, append, paged, fp8, no-alloc)
- * take R <= 32. With the environment variable GQA_DECODE_TC=1, bf16 decode of
- * a contiguous cache at D = 128 with 17..32 rows runs on a tcgen05 kernel
- * instead (same results within the tolerances, same workspace; measured
- * slower on the MQA-end and ragged workloads, so it is off by default).
+ * take R <= 32.
  * A row with no visible key (T_b - sq + s < 0) gets out = 0 and lse = -inf.
  *
  * Device: every pointer is device memory of the current CUDA device (the one
@@ -91,8 +88,8 @@ extern "C" {
  * that no allocation happens during capture. A captured call can be replayed
  * with new contents of the same tensors (values and seq_lens): the plan
  * depends on the shapes only, and the kernels leave the workspace's arrival
- * counters at zero after each merge, so every replay starts from a clean
- * count.
+ * counters at zero after each merge -- also after a call whose bounded wait
+ * expired -- so every replay starts from a clean count.
  *
  * q, k_cache, v_cache, seq_lens, out, lse: device pointers, layouts above.
  * scale: multiplier applied to q.k (1/sqrt(D) for the pages' definition).
