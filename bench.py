@@ -592,6 +592,18 @@ def run_gpu(args, cfg):
     else:
         hkv = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in wl.host_kv]
     dkv = wl.sets[0]
+    copies = list(zip(dkv, hkv))
+    if not args.paged:
+        # A contiguous cache is copied as the rows each (sequence, KV head)
+        # holds: the rows past a sequence's length are never read, so they are
+        # not inputs of the step (block scales: the blocks those rows touch).
+        copies = []
+        for d, h in zip(dkv, hkv):
+            per_block = 64 if (args.fp8 and h.dim() == 3) else 1
+            for b, t in enumerate(wl.lens):
+                n = -(-int(t) // per_block)
+                if n:
+                    copies += [(d[b, g, :n], h[b, g, :n]) for g in range(cfg.G)]
     ho = torch.empty(wl.out.shape, dtype=torch.bfloat16).pin_memory()
     hlse = torch.empty(wl.lse.shape, dtype=torch.float32).pin_memory()
     if args.append:
@@ -600,7 +612,7 @@ def run_gpu(args, cfg):
 
     def e2e_step():
         wl.dq.copy_(hq, non_blocking=True)
-        for d, h in zip(dkv, hkv):
+        for d, h in copies:
             d.copy_(h, non_blocking=True)
         wl.dl.copy_(hl, non_blocking=True)
         if args.append:
@@ -622,11 +634,11 @@ def run_gpu(args, cfg):
     b.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms, e2e_value = aggregate_over_ranks(a.elapsed_time(b) / e2e_steps, wl.nbytes, device=dev)
-    h2d = hq.nbytes + hl.nbytes + sum(h.nbytes for h in hkv)
+    h2d = hq.nbytes + hl.nbytes + sum(h.nbytes for _, h in copies)
     if args.append:
         h2d += hkn.nbytes + hvn.nbytes
     d2h = ho.nbytes + hlse.nbytes
-    del hq, hl, hkv, ho, hlse, dkv
+    del hq, hl, hkv, ho, hlse, dkv, copies
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -681,7 +693,12 @@ def run_gpu(args, cfg):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s",
                     "us_per_step": e2e_ms * 1e3,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "h2d": ("Q, the lengths and the whole paged pool with its block table" if args.paged else
+                            "Q, the lengths and the cache rows each (sequence, KV head) holds"
+                            + (" with their block scales" if args.fp8 else "")
+                            + (" and the new tokens' K/V" if args.append else "")),
+                    "d2h": "out and lse"},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "workloads": workloads,
