@@ -13,6 +13,7 @@
 #include <cstdlib>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "gqa_decode.h"
@@ -39,7 +40,11 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
-std::map<std::pair<int, cudaStream_t>, std::pair<void*, size_t>> g_workspaces;
+// Library-owned buffers per (device, stream, kind). Kind kDecodeWs holds the
+// split-KV arrival counters and partial slots; kind kPrefillWs the prefill's
+// split key-range partials, kept apart so that they never land on counters.
+constexpr int kDecodeWs = 0, kPrefillWs = 1;
+std::map<std::tuple<int, cudaStream_t, int>, std::pair<void*, size_t>> g_workspaces;
 
 int device_info(DeviceInfo* out) {
     int dev = 0;
@@ -308,13 +313,14 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32
     return GQA_OK;
 }
 
-// The library-owned workspace of (current device, stream), grown to `need`.
-int stream_workspace(cudaStream_t stream, size_t need, void** ws, size_t* have) {
+// The library-owned workspace of (current device, stream, kind), grown to
+// `need`.
+int stream_workspace(cudaStream_t stream, size_t need, void** ws, size_t* have, int kind = kDecodeWs) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
     std::lock_guard<std::mutex> lk(g_mu);
-    auto& slot = g_workspaces[{dev, stream}];
+    auto& slot = g_workspaces[{dev, stream, kind}];
     if (slot.second < need) {
         if (slot.first) {
             // The old buffer may still be in use by work queued on this stream.
@@ -474,7 +480,7 @@ int gqa_prefill(const void* q, const void* k_cache, const void* v_cache, const i
     size_t have = 0;
     const size_t need = prefill_workspace_bytes(D, items, (int)splits);
     if (need > 0) {
-        st = stream_workspace(stream, need, &ws, &have);
+        st = stream_workspace(stream, need, &ws, &have, kPrefillWs);
         if (st != GQA_OK) return st;
     }
     PrefillLaunchArgs a{};
@@ -529,16 +535,22 @@ int gqa_decode_release_workspace(cudaStream_t stream) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
     std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_workspaces.find({dev, stream});
-    if (it == g_workspaces.end()) return GQA_OK;
-    // Work already queued on the stream may still use the buffer.
-    e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) return cuda_fail(e);
-    void* buf = it->second.first;
-    g_workspaces.erase(it);
-    if (buf) {
-        e = cudaFree(buf);
-        if (e != cudaSuccess) return cuda_fail(e);
+    bool synced = false;
+    for (int kind : {kDecodeWs, kPrefillWs}) {
+        auto it = g_workspaces.find({dev, stream, kind});
+        if (it == g_workspaces.end()) continue;
+        // Work already queued on the stream may still use the buffer.
+        if (!synced) {
+            e = cudaStreamSynchronize(stream);
+            if (e != cudaSuccess) return cuda_fail(e);
+            synced = true;
+        }
+        void* buf = it->second.first;
+        g_workspaces.erase(it);
+        if (buf) {
+            e = cudaFree(buf);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
     }
     return GQA_OK;
 }

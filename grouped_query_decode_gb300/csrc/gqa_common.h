@@ -175,7 +175,8 @@ struct KernelShape {
     // Dual groups: group 1's per-lane state (m, l partials and the O
     // fragments of each slice) for group 0 to merge.
     static constexpr int kGroupBytes = kDual ? kSlices * 32 * (D / 8 * 4 + 4) * 4 : 0;
-    static constexpr int kBarBytes = 8 * (2 * kStages + 4 * MT + 2) + 64;
+    // + 64: plan words, abort and last flags; + 128: the row table (32 rows).
+    static constexpr int kBarBytes = 8 * (2 * kStages + 4 * MT + 2) + 64 + 128;
     // +1024 so the ring can be aligned to the 1 KB swizzle atom at run time.
     static constexpr int kSmemBytes =
         1024 + kStages * kStageBytes + kMergeBytes + kMlBytes + kQBytes + kGroupBytes + kBarBytes;

@@ -94,34 +94,49 @@ struct SegmentWalkerT {
 using SegmentWalker = SegmentWalkerT<>;
 
 // Counts one arrival on a unit's counter and returns the arrivals so far in
-// this call. The counter holds (epoch << 16) | count; the first arrival of a
-// call finds another epoch there and restarts the count, so the workspace
-// never needs clearing. A CAS only fails when another CTA's CAS succeeded, so
-// the loop ends; it is bounded all the same.
+// this call. The counter holds (epoch << 16) | count. An arrival adds one;
+// when the tag it finds is this call's, the count it returns is exact in
+// that one atomic. Otherwise the word is another call's (or bytes the
+// workspace held before): the arrival then restarts the count under this
+// call's tag, or counts itself once the tag is there, with compare-and-swap
+// (its add on the old word is overwritten, and so not counted twice). So
+// the workspace never needs clearing. A CAS only fails when another CTA
+// changed the word, so the loop ends; it is bounded all the same.
 __device__ __forceinline__ unsigned arrive_unit(unsigned long long* ctr, unsigned long long epoch,
                                                 unsigned* status) {
-    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr);
+    const unsigned long long old = atomicAdd(ctr, 1ull);
+    if ((old >> 16) == epoch) return (unsigned)(old & 0xffffu) + 1u;
+    unsigned long long cur = old + 1ull;
     for (int i = 0; i < (1 << 20); ++i) {
-        const unsigned long long next = ((old >> 16) == epoch) ? old + 1 : ((epoch << 16) | 1ull);
-        const unsigned long long prev = atomicCAS(ctr, old, next);
-        if (prev == old) return (unsigned)(next & 0xffffu);
-        old = prev;
+        const unsigned long long next = ((cur >> 16) == epoch) ? cur + 1 : ((epoch << 16) | 1ull);
+        const unsigned long long prev = atomicCAS(ctr, cur, next);
+        if (prev == cur) return (unsigned)(next & 0xffffu);
+        cur = prev;
     }
     atomicOr(status, kStatusTimeout);
     return 0;
 }
 
-// The arrival that completes a unit's count resets its counter: a launch
-// replayed from a CUDA graph carries the epoch of the call that was captured,
-// so the next replay must find the count at zero (a zero counter matches no
-// epoch, so a call outside a graph restarts it as before). No other CTA of
-// the launch touches the counter after the last arrival.
-__device__ __forceinline__ void release_unit(unsigned long long* ctr) { atomicExch(ctr, 0ull); }
+// The arrival that completes a unit's count sets the count back to zero
+// under the call's tag: a launch replayed from a CUDA graph carries the tag
+// of the call that was captured, so the next replay counts from zero, every
+// arrival in one atomic. No other CTA of the launch touches the counter
+// after the last arrival.
+__device__ __forceinline__ void release_unit(unsigned long long* ctr, unsigned long long epoch) {
+    atomicExch(ctr, epoch << 16);
+}
+
+// a / b for a >= 0, b > 0: the 32-bit unsigned division when both fit (every
+// workload here), a far shorter instruction sequence than the 64-bit one.
+__device__ __forceinline__ long long div_nonneg(long long a, long long b) {
+    if (((unsigned long long)a | (unsigned long long)b) >> 32) return a / b;
+    return (long long)((unsigned)a / (unsigned)b);
+}
 
 // The CTA holding tile x, and CTA c's share, for the equal partition of W
 // tiles over P CTAs.
 __device__ __forceinline__ long long cta_of_tile(long long x, long long W, long long P) {
-    return ((x + 1) * P - 1) / W;
+    return div_nonneg((x + 1) * P - 1, W);
 }
 
 // CTAs that hold a share of the unit whose tiles are [ub, ue): with at least
@@ -131,7 +146,7 @@ __device__ __forceinline__ unsigned unit_contributors(long long ub, long long ue
     const long long cf = cta_of_tile(ub, W, P), cl = cta_of_tile(ue - 1, W, P);
     if (W >= P) return (unsigned)(cl - cf + 1);
     unsigned n = 0;
-    for (long long c = cf; c <= cl; ++c) n += (c * W / P) < ((c + 1) * W / P) ? 1u : 0u;
+    for (long long c = cf; c <= cl; ++c) n += div_nonneg(c * W, P) < div_nonneg((c + 1) * W, P) ? 1u : 0u;
     return n;
 }
 
@@ -141,9 +156,8 @@ __device__ __forceinline__ bool arrive_and_release(const DecodeParams& p, const 
                                                    long long P) {
     unsigned long long* ctr = p.ws_counters + ((size_t)s.b * p.G + s.g) * kMaxRowTiles + mt;
     const unsigned contributors = unit_contributors(s.ub, s.ue, W, P);
-    const unsigned arrived = arrive_unit(ctr, p.epoch, p.status);
-    if (arrived != contributors) return false;
-    release_unit(ctr);
+    if (arrive_unit(ctr, p.epoch, p.status) != contributors) return false;
+    release_unit(ctr, p.epoch);
     return true;
 }
 
@@ -375,7 +389,7 @@ __device__ __forceinline__ void plan_share_small(const DecodeParams& p, int lane
     }
     int bstart = p.B, prestart = total;
     if ((int)blockIdx.x < P) {
-        const int lo = (int)(((long long)blockIdx.x * total) / P);
+        const int lo = (int)div_nonneg((long long)blockIdx.x * total, P);
         const unsigned hit0 = __ballot_sync(0xffffffffu, has0 && s0 > lo);
         const unsigned hit1 = __ballot_sync(0xffffffffu, has1 && tot0 + s1 > lo);
         if (hit0) {
@@ -504,6 +518,9 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     long long* shared_ll = reinterpret_cast<long long*>(bars + 2 * S + 4 * MT + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(shared_ll + 4);
     volatile int* last_flag = abort_flag + 1;              // [MT]
+    // Row r of a KV head's R rows: (new token s << 16) | head j within the
+    // group, r = j * sq + s; written once so that no segment divides by sq.
+    int* rowtab = reinterpret_cast<int*>(shared_ll + 8);   // [kMaxRowTiles * 16]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -526,6 +543,10 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
     }
+    if (threadIdx.x >= 32 && threadIdx.x < 32 + p.R) {
+        const int r = threadIdx.x - 32;
+        rowtab[r] = ((r % p.sq) << 16) | (r / p.sq);
+    }
     // Inputs may be written by the previous grid in the stream.
     pdl_wait_primary();
 
@@ -545,8 +566,8 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     walk.seq_lens = p.seq_lens;
     walk.G = p.G;
     walk.Tmax = p.Tmax;
-    walk.lo = (long long)blockIdx.x < P ? (long long)blockIdx.x * W / P : W;
-    walk.hi = (long long)blockIdx.x < P ? (long long)(blockIdx.x + 1) * W / P : W;
+    walk.lo = (long long)blockIdx.x < P ? div_nonneg((long long)blockIdx.x * W, P) : W;
+    walk.hi = (long long)blockIdx.x < P ? div_nonneg((long long)(blockIdx.x + 1) * W, P) : W;
     walk.x = walk.lo;
     walk.b = (int)shared_ll[1];
     walk.pre_b = shared_ll[2];
@@ -656,13 +677,13 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             const uint16_t* q_lo = nullptr;
             const uint16_t* q_hi = nullptr;
             if (r_lo < p.R) {
-                const int j = r_lo / p.sq, s = r_lo % p.sq;
+                const int e = rowtab[r_lo], j = e & 0xffff, s = e >> 16;
                 out_lo = (sg.b * p.sq + s) * p.H + sg.g * p.heads_per_group + j;
                 q_lo = p.q + (size_t)out_lo * D;
                 lim_lo = sg.tb - p.sq + s;
             }
             if (r_hi < p.R) {
-                const int j = r_hi / p.sq, s = r_hi % p.sq;
+                const int e = rowtab[r_hi], j = e & 0xffff, s = e >> 16;
                 out_hi = (sg.b * p.sq + s) * p.H + sg.g * p.heads_per_group + j;
                 q_hi = p.q + (size_t)out_hi * D;
                 lim_hi = sg.tb - p.sq + s;
@@ -711,7 +732,7 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                         qa4[u] = make_uint4(0u, 0u, 0u, 0u);
                         qb4[u] = qa4[u];
                         if (r < p.R) {
-                            const int j = r / p.sq, sq_i = r % p.sq;
+                            const int e = rowtab[r], j = e & 0xffff, sq_i = e >> 16;
                             const int qrow = (sg.b * p.sq + sq_i) * p.H + sg.g * p.heads_per_group + j;
                             const uint4* src = reinterpret_cast<const uint4*>(p.q + (size_t)qrow * D) + 2 * c16;
                             qa4[u] = __ldg(src);
@@ -740,7 +761,7 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                         const int r = mt * 16 + row;
                         v[u] = make_uint4(0u, 0u, 0u, 0u);
                         if (r < p.R) {
-                            const int j = r / p.sq, sq_i = r % p.sq;
+                            const int e = rowtab[r], j = e & 0xffff, sq_i = e >> 16;
                             const int qrow = (sg.b * p.sq + sq_i) * p.H + sg.g * p.heads_per_group + j;
                             v[u] = __ldg(reinterpret_cast<const uint4*>(p.q + (size_t)qrow * D) + chunk);
                         }
@@ -1262,7 +1283,7 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             // CTA after cf this unit is where its share starts; cf's share
             // starts at the unit's first tile exactly when cf * W / P == ub.
             const int ncand = (int)(cl - cf + 1);
-            const int first_slot = (int)(cf * 2 + ((cf * W / P) == sg.ub ? 0 : 1));
+            const int first_slot = (int)(cf * 2 + (div_nonneg(cf * W, P) == sg.ub ? 0 : 1));
             const int rows_here = (p.R - mt * 16) < 16 ? (p.R - mt * 16) : 16;
             // NC candidate slots held per item, NI items of this thread merged
             // from one round of loads (up to four with at most two
@@ -1315,7 +1336,7 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                             acc.w += w * ok4[u][k].w;
                         }
                         const float inv = L > 0.f ? 1.f / L : 0.f;
-                        const int j = r / p.sq, s = r % p.sq;
+                        const int e = rowtab[r], j = e & 0xffff, s = e >> 16;
                         const int row = (sg.b * p.sq + s) * p.H + sg.g * p.heads_per_group + j;
                         *reinterpret_cast<uint2*>(p.out + (size_t)row * D + c4) =
                             make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
@@ -1347,8 +1368,8 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             const int rows_here = (p.R - mt * 16) < 16 ? (p.R - mt * 16) : 16;
             for (int k = tid_mt; k < ncand; k += kSlices * 32) {
                 const long long c = cf + k;
-                const long long clo = c * W / P;
-                slot_of[k] = clo < (c + 1) * W / P ? (int)(c * 2 + (clo >= sg.ub ? 0 : 1)) : -1;
+                const long long clo = div_nonneg(c * W, P);
+                slot_of[k] = clo < div_nonneg((c + 1) * W, P) ? (int)(c * 2 + (clo >= sg.ub ? 0 : 1)) : -1;
             }
             mbar_arrive(mbarD);
             if (!wait_phase(mbarD, d_parity, abort_flag, p.status, tmo)) { failed = true; break; }
@@ -1386,7 +1407,7 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                 for (int k = lane; k < ncand; k += 32) wts[k * 16 + rr] *= inv;
                 if (lane == 0 && p.lse) {
                     const int r = mt * 16 + rr;
-                    const int j = r / p.sq, s = r % p.sq;
+                    const int e = rowtab[r], j = e & 0xffff, s = e >> 16;
                     const int row = (sg.b * p.sq + s) * p.H + sg.g * p.heads_per_group + j;
                     p.lse[row] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
                 }
@@ -1412,7 +1433,7 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
                     acc.z += w * v.z;
                     acc.w += w * v.w;
                 }
-                const int j = r / p.sq, s = r % p.sq;
+                const int e = rowtab[r], j = e & 0xffff, s = e >> 16;
                 const int row = (sg.b * p.sq + s) * p.H + sg.g * p.heads_per_group + j;
                 uint2 packed;
                 packed.x = pack_bf16x2(acc.x, acc.y);

@@ -220,7 +220,7 @@ typedef struct gqa_decode_plan_t {
     int tile_tokens;       /* tokens per pipeline stage */
     int row_tiles;         /* 16-row MMA tiles per KV head: ceil(R / 16) */
     int stages;            /* depth of the shared-memory K/V ring */
-    int threads;           /* threads per CTA (consumer warps + 1 producer warp) */
+    int threads;           /* threads per CTA (consumer, producer and page-loader warps) */
     int smem_bytes;        /* dynamic shared memory per CTA */
     long long max_tiles;   /* B * G * ceil(Tmax / tile_tokens): tiles if every T_b = Tmax */
 } gqa_decode_plan_t;
@@ -269,9 +269,10 @@ int gqa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                        int B, int sq, int H, int G, int D, int Tmax, cudaStream_t stream);
 
 /*
- * Frees the workspace the library owns for (current device, `stream`), the
- * one gqa_decode, gqa_decode_append, gqa_decode_paged, gqa_decode_fp8 and
- * gqa_prefill grow on that stream. Call it before destroying a stream that
+ * Frees the workspace the library owns for (current device, `stream`): the
+ * buffer gqa_decode, gqa_decode_append, gqa_decode_paged and gqa_decode_fp8
+ * grow on that stream, and the separate one of gqa_prefill's split key
+ * ranges. Call it before destroying a stream that
  * the library was used on, or to give the memory back; a later call on the
  * stream allocates again. It synchronises `stream` first (work already
  * queued may use the buffer). Returns GQA_OK (also when the library holds

@@ -157,7 +157,8 @@ def test_explicit_workspace_matches_library_workspace():
 def test_explicit_workspace_guard_words():
     """Canary bytes on both sides of a caller-owned workspace stay untouched by
     a call whose plan splits units over many CTAs (every CTA writes partial
-    slots, the counters are used), and the result matches the oracle."""
+    slots, the counters are used), and the result matches the oracle. The
+    workspace starts as those canary bytes too: it needs no clearing."""
     B, sq, H, G, D, Tmax = 3, 4, 64, 8, 128, 900
     q, k, v, lens = make_inputs(B, sq, H, G, D, Tmax, [900, 517, 77], seed=208)
     dq, dk, dv = to_device_bf16(q), to_device_bf16(k), to_device_bf16(v)
@@ -178,6 +179,24 @@ def test_explicit_workspace_guard_words():
     assert np.all(host[:guard] == 0xA5) and np.all(host[guard + nbytes:] == 0xA5), "workspace guard"
     ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, 1 / math.sqrt(D), threads=8)
     compare(bf16_to_f64(out), lse.cpu().numpy().astype(np.float64), ref_out, ref_lse, what="guarded workspace")
+
+
+def test_prefill_partials_leave_the_decode_counters_alone():
+    """A short prefill chunk whose key ranges are split writes its partials
+    into a library buffer of its own, not over the decode workspace's arrival
+    counters: a split-KV decode on the same stream right after it matches the
+    oracle with a clean status word, and so does the prefill."""
+    B, sq, H, G, D, Tmax = 1, 64, 8, 2, 128, 2048
+    q, k, v, lens = make_inputs(B, sq, H, G, D, Tmax, [2048], seed=212)
+    scale = 1 / math.sqrt(D)
+    ref_out, ref_lse = oracle.gqa_decode_f64(q, k, v, lens, scale, threads=8)
+    out, lse = run_gpu(q, k, v, lens, scale, entry=gq.gqa_prefill)
+    compare(out, lse, ref_out, ref_lse, what="split prefill")
+    q2, k2, v2, lens2 = make_inputs(3, 1, 32, 8, 128, 700, [700, 650, 129], seed=213)
+    ref2 = oracle.gqa_decode_f64(q2, k2, v2, lens2, scale, threads=8)
+    with min_tiles(1):
+        out2, lse2 = run_gpu(q2, k2, v2, lens2, scale)   # checks the status word
+    compare(out2, lse2, *ref2, what="decode after split prefill")
 
 
 def test_release_workspace_frees_and_the_next_call_allocates_again():
