@@ -178,6 +178,29 @@ unsigned long long call_epoch() {
     return e > 0 ? (unsigned long long)e & 0xFFFFFFFFFFFFull : next_epoch();
 }
 
+// When every unit has the same number of tiles (all lengths equal; the
+// kernel checks that from the lengths), the tiles are shared by fewer CTAs
+// if a grid that keeps at least 80% of them busy lines up with the units: a
+// whole number of units per CTA (no unit split, nothing to merge), or, with
+// fewer units than CTAs, the same whole number of CTAs per unit (every CTA
+// one equal partial) on about 85% of the grid. Measured on the long-context
+// and MQA-end workloads: about 85% of the SMs, each unit split evenly, beats
+// every SM with uneven splits (fewer partials, HBM still saturated). The
+// CTAs left over exit. Computed here, once per call, rather than by every
+// CTA before its first copy.
+int even_split_ctas(long long units, int ctas) {
+    long long P = ctas;
+    if (units >= P) {
+        const long long per = (units + P - 1) / P;
+        const long long even = (units + per - 1) / per;
+        if (units % per == 0 && 5 * even >= 4 * P) P = even;
+    } else {
+        const long long even = units * ((P * 85 / 100) / units);
+        if (even >= units && 5 * even >= 4 * P) P = even;
+    }
+    return (int)P;
+}
+
 // Grid size override for sweeps of the plan (unset: the heuristic decides).
 int forced_ctas() {
     const char* s = std::getenv("GQA_DECODE_CTAS");
@@ -291,6 +314,7 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32
     a.p.heads_per_group = H / G;
     a.p.ctas = plan.ctas;
     a.p.even_rule = forced_ctas() > 0 ? 0 : 1;
+    a.p.even_ctas = even_split_ctas((long long)B * G, plan.ctas);
     a.p.small_plan = (B <= 64 && plan.max_tiles < (1ll << 31)) ? 1 : 0;
     debug_knobs(&a.p.wait_timeout_ns, &a.p.skip_tile);
     a.p.k_new = static_cast<const uint16_t*>(k_new);

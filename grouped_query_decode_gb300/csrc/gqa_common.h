@@ -53,7 +53,8 @@ struct DecodeParams {
     unsigned long long wait_timeout_ns;  // limit of every device-side wait
     float scale_log2;        // scale * log2(e)
     int B, sq, H, G, Tmax, R, heads_per_group, ctas;
-    int even_rule;           // 1: use fewer CTAs when that splits no unit (see kernel)
+    int even_rule;           // 1: with equal tile counts, even_ctas CTAs share the tiles
+    int even_ctas;           // the CTAs of the equal-length rule (host-computed, see api.cu)
     int small_plan;          // 1: B <= 64 and B * G * ceil(Tmax / 64) < 2^31 (32-bit plan)
     int skip_tile;           // fault injection for tests: CTA 0 never loads its tile
                              // number skip_tile (-1: off), so its consumers' wait expires

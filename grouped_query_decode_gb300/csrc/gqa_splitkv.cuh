@@ -343,12 +343,8 @@ struct TileIssuer {
 // sequences i, i+32, ... of the first 256.
 //
 // When every unit has the same number of tiles (all lengths equal), the
-// tiles are shared by fewer CTAs if a grid that keeps at least 80% of
-// them busy lines up with the units: a whole number of units per CTA (no
-// unit split, nothing to merge), or, with fewer units than CTAs, the same
-// whole number of CTAs per unit (every CTA one equal partial) on about 85%
-// of the grid (kSplitEven; a kernel whose merges are cheap keeps every CTA).
-// The CTAs left over exit.
+// tiles are shared by p.even_ctas CTAs (the host's equal-length rule: a
+// grid that lines up with the units); the CTAs left over exit.
 // plan_share for up to 64 sequences and fewer than 2^31 tiles in all
 // (DecodeParams::small_plan, set by the host from B and B * G *
 // ceil(Tmax / 64)): lane i holds sequences i and i + 32, and every sum is a
@@ -375,18 +371,7 @@ __device__ __forceinline__ void plan_share_small(const DecodeParams& p, int lane
     const unsigned big = 0x7fffffffu;
     const int nt_min = (int)__reduce_min_sync(0xffffffffu, min(has0 ? (unsigned)n0 : big, has1 ? (unsigned)n1 : big));
     const int nt_max = (int)__reduce_max_sync(0xffffffffu, (unsigned)max(n0, n1));
-    int P = p.ctas;
-    if (p.even_rule && nt_min == nt_max && nt_max > 0) {
-        const int units = p.B * p.G;
-        if (units >= P) {
-            const int per = (units + P - 1) / P;
-            const int even = (units + per - 1) / per;
-            if (units % per == 0 && 5 * even >= 4 * P) P = even;
-        } else {
-            const int even = units * ((P * 85 / 100) / units);
-            if (even >= units && 5 * even >= 4 * P) P = even;
-        }
-    }
+    const int P = (p.even_rule && nt_min == nt_max && nt_max > 0) ? p.even_ctas : p.ctas;
     int bstart = p.B, prestart = total;
     if ((int)blockIdx.x < P) {
         const int lo = (int)div_nonneg((long long)blockIdx.x * total, P);
@@ -410,7 +395,7 @@ __device__ __forceinline__ void plan_share_small(const DecodeParams& p, int lane
     }
 }
 
-template <int TT, bool kSplitEven = true>
+template <int TT>
 __device__ __forceinline__ void plan_share(const DecodeParams& p, int lane, long long* shared_ll) {
     constexpr int kCached = 8;       // sequences 0..255 stay in registers
     long long cached[kCached];
@@ -447,21 +432,7 @@ __device__ __forceinline__ void plan_share(const DecodeParams& p, int lane, long
         total += __shfl_sync(0xffffffffu, scan_add(tiles_times_g(b0 + lane)), 31);
     nt_min = __reduce_min_sync(0xffffffffu, nt_min);
     nt_max = __reduce_max_sync(0xffffffffu, nt_max);
-    long long P = p.ctas;
-    if (p.even_rule && nt_min == nt_max && nt_max > 0) {
-        const long long units = (long long)p.B * p.G;
-        if (units >= P) {
-            const long long per = (units + P - 1) / P;
-            const long long even = (units + per - 1) / per;
-            if (units % per == 0 && 5 * even >= 4 * P) P = even;
-        } else if (kSplitEven) {
-            // Measured on the long-context and MQA-end workloads: about
-            // 85% of the SMs, each unit split evenly, beats every SM with
-            // uneven splits (fewer partials, HBM still saturated).
-            const long long even = units * ((P * 85 / 100) / units);
-            if (even >= units && 5 * even >= 4 * P) P = even;
-        }
-    }
+    const long long P = (p.even_rule && nt_min == nt_max && nt_max > 0) ? p.even_ctas : p.ctas;
     // First sequence whose tiles reach past lo, and the tiles before it.
     const long long lo = (long long)blockIdx.x * total / P;
     long long pre = 0;
