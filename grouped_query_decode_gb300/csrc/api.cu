@@ -315,6 +315,14 @@ int enqueue(const void* q, const void* k_cache, const void* v_cache, const int32
     a.p.ctas = plan.ctas;
     a.p.even_rule = forced_ctas() > 0 ? 0 : 1;
     a.p.even_ctas = even_split_ctas((long long)B * G, plan.ctas);
+    // Kernels bound per SM rather than by HBM take every SM: pages shorter
+    // than a tile (the TMA boxes per tile bound each SM: the MHA end's
+    // layer in 16-token pages 122 -> 109 us on all 152 SMs instead of 128),
+    // and fp8 caches with fewer units than half the SMs (long context B = 1
+    // 63 -> 59 us). With more units, whole units per CTA keep fp8's merges
+    // away (the Llama-shaped layer: 28.7 us on 128 CTAs, 32.2 on 152).
+    const bool short_pages = pg.block_table && pg.page_size < kTileTokens;
+    if (short_pages || (kv8 && 2ll * B * G < plan.ctas)) a.p.even_ctas = plan.ctas;
     a.p.small_plan = (B <= 64 && plan.max_tiles < (1ll << 31)) ? 1 : 0;
     debug_knobs(&a.p.wait_timeout_ns, &a.p.skip_tile);
     a.p.k_new = static_cast<const uint16_t*>(k_new);

@@ -10,7 +10,7 @@ import torch
 import grouped_query_decode_gb300 as gq
 import oracle
 import synthetic as syn
-from gpu_helpers import bf16_to_f64, compare, run_gpu, to_device_bf16
+from gpu_helpers import bf16_to_f64, compare, env, run_gpu, to_device_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -52,11 +52,19 @@ def test_fp8_full_size_sampled_units(name):
 @pytest.mark.parametrize("name,page_size", [("llama3_8b_layer", 16), ("llama3_8b_layer", 256), ("mqa_end", 16)])
 def test_paged_full_size_equals_contiguous(name, page_size):
     """One row tile (page-major stage at 16-token pages) and two row tiles
-    (MQA end: block-major stage)."""
+    (MQA end: block-major stage). Pages shorter than a tile take every SM
+    (no equal-length grid rule), so the contiguous call that must give the
+    same bits runs on that grid too (GQA_DECODE_CTAS = the SM count); it is
+    also within the parity bar of the contiguous call on its own grid."""
     cfg = syn.config_by_name(name)
     q, k, v, lens = syn.make_inputs(cfg, threads=16)
     kp, vp, table = syn.paginate(k, v, lens, page_size, seed=cfg.seed + 100)
-    cont_out, cont_lse = run_gpu(q, k, v, lens, cfg.scale)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    with env(GQA_DECODE_CTAS=sms if page_size < 64 else None):
+        cont_out, cont_lse = run_gpu(q, k, v, lens, cfg.scale)
+    if page_size < 64:
+        own_out, own_lse = run_gpu(q, k, v, lens, cfg.scale)
+        compare(cont_out, cont_lse, own_out, own_lse, what=f"{name} all-SM grid vs its own")
     out = torch.empty(cfg.B, cfg.sq, cfg.H, cfg.D, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(cfg.B, cfg.sq, cfg.H, dtype=torch.float32, device="cuda")
     gq.gqa_decode_paged(to_device_bf16(q), to_device_bf16(kp), to_device_bf16(vp),
