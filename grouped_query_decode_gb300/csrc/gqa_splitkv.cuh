@@ -349,8 +349,7 @@ struct TileIssuer {
 // (DecodeParams::small_plan, set by the host from B and B * G *
 // ceil(Tmax / 64)): lane i holds sequences i and i + 32, and every sum is a
 // 32-bit scan. Same result as plan_share; it exists because every kernel
-// launch pays for the plan before its first copy, in instruction fetches
-// of cold code more than in arithmetic, so the plan is kept short.
+// launch pays for the plan before its first copy, so the plan is kept short.
 template <int TT>
 __device__ __forceinline__ void plan_share_small(const DecodeParams& p, int lane, long long* shared_ll) {
     const bool has0 = lane < p.B, has1 = lane + 32 < p.B;
@@ -1257,8 +1256,10 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             const int first_slot = (int)(cf * 2 + (div_nonneg(cf * W, P) == sg.ub ? 0 : 1));
             const int rows_here = (p.R - mt * 16) < 16 ? (p.R - mt * 16) : 16;
             // NC candidate slots held per item, NI items of this thread merged
-            // from one round of loads (up to four with at most two
-            // contributors, the common split of a unit over two CTAs).
+            // from one round of loads: up to four with at most two
+            // contributors (the common split of a unit over two CTAs), two
+            // with up to 16 where the registers hold them (long context
+            // B = 1: 16 CTAs per unit, 86.1 -> 84.4 us), else one.
             auto merge_items = [&](auto nc_c, auto ni_c) {
                 constexpr int NC = decltype(nc_c)::value, NI = decltype(ni_c)::value;
                 constexpr int C4 = D / 4;
@@ -1317,6 +1318,8 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
             };
             if (ncand <= 2)
                 merge_items(IntC<2>{}, IntC<4>{});
+            else if (KS::kFastMerge >= 16 && ncand <= 16)
+                merge_items(IntC<(KS::kFastMerge >= 16 ? 16 : 2)>{}, IntC<2>{});
             else
                 merge_items(IntC<KS::kFastMerge>{}, IntC<1>{});
             continue;
