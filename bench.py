@@ -597,13 +597,24 @@ def run_gpu(args, cfg):
         # A contiguous cache is copied as the rows each (sequence, KV head)
         # holds: the rows past a sequence's length are never read, so they are
         # not inputs of the step (block scales: the blocks those rows touch).
+        # Runs of sequences whose rows fill the cache are one contiguous copy.
         copies = []
         for d, h in zip(dkv, hkv):
             per_block = 64 if (args.fp8 and h.dim() == 3) else 1
-            for b, t in enumerate(wl.lens):
-                n = -(-int(t) // per_block)
+            full = h.shape[2]
+            b = 0
+            while b < cfg.B:
+                n = -(-int(wl.lens[b]) // per_block)
+                if n >= full:
+                    e = b
+                    while e < cfg.B and -(-int(wl.lens[e]) // per_block) >= full:
+                        e += 1
+                    copies.append((d[b:e], h[b:e]))
+                    b = e
+                    continue
                 if n:
                     copies += [(d[b, g, :n], h[b, g, :n]) for g in range(cfg.G)]
+                b += 1
     ho = torch.empty(wl.out.shape, dtype=torch.bfloat16).pin_memory()
     hlse = torch.empty(wl.lse.shape, dtype=torch.float32).pin_memory()
     if args.append:
