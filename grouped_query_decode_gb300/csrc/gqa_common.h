@@ -99,10 +99,10 @@ struct PrefillParams {
 };
 
 // One CTA per SM. Every 16-row tile of the group has four consumer warps
-// ("slices") that take 16 of a stage's 64 tokens each; one more warp issues
-// the TMA copies. With two row tiles (9 warps, which the register file
-// allocates as 12) a thread gets 168 registers, so those warps keep their Q
-// fragments in shared memory rather than in registers.
+// ("slices"); one more warp issues the TMA copies, and (bf16) two more issue
+// the boxes of pages shorter than a tile. With two row tiles (11 warps, which
+// the register file allocates as 12) a thread gets 168 registers, so those
+// warps keep their Q fragments in shared memory rather than in registers.
 template <int D, int MT, bool KV8 = false>
 struct KernelShape {
     // fp8 with one row tile: two groups of four consumer warps take
