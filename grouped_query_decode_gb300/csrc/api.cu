@@ -538,6 +538,9 @@ int gqa_prefill(const void* q, const void* k_cache, const void* v_cache, const i
     a.p.splits = (int)splits;
     a.p.ws_part = static_cast<float*>(ws);
     a.grid = (unsigned)(items * splits);   // (pair of row tiles, key range)
+    // The combine of a split chunk (always one wave of CTAs) launches with
+    // programmatic dependent launch.
+    a.pdl = a.grid <= (unsigned)info.sms;
     a.stream = stream;
     cudaError_t e = launch_prefill(D, a);
     if (e != cudaSuccess) return cuda_fail(e);

@@ -31,6 +31,7 @@ struct PrefillLaunchArgs {
     PrefillParams p;
     unsigned grid;
     cudaStream_t stream;
+    bool pdl;        // the combine: launch with programmatic stream serialization
 };
 cudaError_t launch_prefill(int D, const PrefillLaunchArgs& a);   // + the combine when split
 size_t prefill_workspace_bytes(int D, long long items, int splits);

@@ -581,6 +581,9 @@ __global__ void __launch_bounds__(PrefillShape<D>::kThreads, 1)
 // lane D/32 columns.
 template <int D>
 __global__ void __launch_bounds__(256) gqa_prefill_combine(const PrefillParams p) {
+    // The partials are the previous grid's (programmatic dependent launch).
+    pdl_wait_primary();
+    pdl_launch_dependents();
     constexpr int kStride = prefill_part_stride(D);
     constexpr int kPer = D / 32;
     const int units = p.B * p.G;
