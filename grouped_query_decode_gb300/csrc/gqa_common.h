@@ -99,10 +99,10 @@ struct PrefillParams {
 };
 
 // One CTA per SM. Every 16-row tile of the group has four consumer warps
-// ("slices"); one more warp issues the TMA copies, and (bf16) two more issue
-// the boxes of pages shorter than a tile. With two row tiles (11 warps, which
-// the register file allocates as 12) a thread gets 168 registers, so those
-// warps keep their Q fragments in shared memory rather than in registers.
+// ("slices"); one more warp issues the TMA copies, (bf16) two more issue the
+// boxes of pages shorter than a tile, and one tags the arrival counters. With
+// two row tiles (12 warps) a thread gets 168 registers, so those warps keep
+// their Q fragments in shared memory rather than in registers.
 template <int D, int MT, bool KV8 = false>
 struct KernelShape {
     // fp8 with one row tile: two groups of four consumer warps take
@@ -127,7 +127,11 @@ struct KernelShape {
     // cost no registers: the register file is allocated in steps of four
     // warps (5 -> 8 and 9 -> 12 either way).
     static constexpr int kLoaderWarps = KV8 ? 0 : 2;
-    static constexpr int kThreads = (kConsumerWarps + 1 + kLoaderWarps) * 32;
+    // The last warp gives the arrival counters of the CTA's partial units the
+    // call's tag before any arrival (see the kernel). Every shape has a free
+    // slot for it in its allocation step: 8 -> 8, 11 -> 12, 9 -> 10 of 12.
+    static constexpr int kCounterWarp = kConsumerWarps + 1 + kLoaderWarps;
+    static constexpr int kThreads = (kCounterWarp + 1) * 32;
     // Registers per thread: the 64K register file for one CTA, with warps
     // counted in the allocation steps of 4, in steps of 8 registers, <= 255.
     static constexpr int kAllocWarps = (kThreads / 32 + 3) / 4 * 4;

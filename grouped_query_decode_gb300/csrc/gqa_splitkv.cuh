@@ -117,6 +117,22 @@ __device__ __forceinline__ unsigned arrive_unit(unsigned long long* ctr, unsigne
     return 0;
 }
 
+// Gives a unit's counter this call's tag with a zero count if it holds another
+// tag, and leaves a word with this call's tag alone. It is not an arrival:
+// an arrival whose add landed on the old word counts itself again under the
+// new tag (arrive_unit), so overwriting that add loses nothing. Done early by
+// the counter warp, it lets the arrivals at the segments' ends take the one-
+// add path instead of contending in compare-and-swap loops. Bounded; if it
+// gives up, the arrivals retag as before.
+__device__ __forceinline__ void retag_unit(unsigned long long* ctr, unsigned long long epoch) {
+    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
+    for (int i = 0; i < 64 && (cur >> 16) != epoch; ++i) {
+        const unsigned long long prev = atomicCAS(ctr, cur, epoch << 16);
+        if (prev == cur) return;
+        cur = prev;
+    }
+}
+
 // The arrival that completes a unit's count sets the count back to zero
 // under the call's tag: a launch replayed from a CUDA graph carries the tag
 // of the call that was captured, so the next replay counts from zero, every
@@ -545,6 +561,24 @@ __global__ void __maxnreg__((KernelShape<D, MT, KV8>::kMaxRegs))
     walk.x = walk.lo;
     walk.b = (int)shared_ll[1];
     walk.pre_b = shared_ll[2];
+
+    if (warp == KS::kCounterWarp) {
+        // ------------------------------------------ counter warp
+        // Before the first segment ends, the counters of every partial unit
+        // of this CTA's share (lane mt: row tile mt's) get this call's tag.
+        // Without it the first arrivals of a unit each found the previous
+        // call's tag and retagged in a compare-and-swap loop: with 16-19
+        // CTAs a unit arriving together (long context B = 1) that chain of
+        // retries took up to 10 us.
+        if (lane < MT) {
+            SegmentWalker w = walk;
+            Segment sg;
+            while (w.next(sg))
+                if (!sg.complete)
+                    retag_unit(p.ws_counters + ((size_t)sg.b * p.G + sg.g) * kMaxRowTiles + lane, p.epoch);
+        }
+        return;
+    }
 
     if (warp > KS::kConsumerWarps) {
         // ------------------------------------------ second and third issuers

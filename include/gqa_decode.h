@@ -220,7 +220,7 @@ typedef struct gqa_decode_plan_t {
     int tile_tokens;       /* tokens per pipeline stage */
     int row_tiles;         /* 16-row MMA tiles per KV head: ceil(R / 16) */
     int stages;            /* depth of the shared-memory K/V ring */
-    int threads;           /* threads per CTA (consumer, producer and page-loader warps) */
+    int threads;           /* threads per CTA (consumer, producer, page-loader and counter warps) */
     int smem_bytes;        /* dynamic shared memory per CTA */
     long long max_tiles;   /* B * G * ceil(Tmax / tile_tokens): tiles if every T_b = Tmax */
 } gqa_decode_plan_t;

@@ -45,12 +45,12 @@ def test_plan_shapes():
     p = gq.gqa_decode_plan(16, 1, 32, 8, 128, 4096, 152)
     assert p["ctas"] == 152 and p["tile_tokens"] == 64 and p["row_tiles"] == 1
     assert p["max_tiles"] == 16 * 8 * 64
-    # 4 consumer warps, the producer warp and the two page-loader warps
-    # (idle unless the cache is paged in pages shorter than a tile).
-    assert p["smem_bytes"] <= 227 * 1024 and p["threads"] == 224
-    # MQA end: 32 rows -> two 16-row tiles: 8 consumer warps + producer + 2 loaders.
+    # 4 consumer warps, the producer warp, the two page-loader warps (idle
+    # unless the cache is paged in pages shorter than a tile), the counter warp.
+    assert p["smem_bytes"] <= 227 * 1024 and p["threads"] == 256
+    # MQA end: 32 rows -> two 16-row tiles: 8 consumers + producer + 2 loaders + counter.
     p = gq.gqa_decode_plan(64, 1, 32, 1, 128, 8192, 152)
-    assert p["row_tiles"] == 2 and p["threads"] == 352
+    assert p["row_tiles"] == 2 and p["threads"] == 384
     # A tiny problem gets at least 16 tiles (1024 tokens) per CTA.
     p = gq.gqa_decode_plan(1, 1, 32, 8, 64, 1024, 152)
     assert p["max_tiles"] == 128 and p["ctas"] == 8

@@ -14,7 +14,8 @@ every kind of starting word, and checks that exactly one arrival sees the
 full count (it is the last one to start, so every partial was written
 before it), that every arrival count 1..n is handed out once, and that the
 word ends at (epoch << 16) | 0, which the next call, or a replay with the
-same tag, counts from. A negative control shows that a plain add, without
+same tag, counts from; also with the kernel's counter warps retagging the
+word at the same time. A negative control shows that a plain add, without
 the retag, miscounts on a word left by another call.
 """
 import random
@@ -47,6 +48,23 @@ def _arrival(epoch, mem, log, name):
     raise AssertionError("CAS loop did not end")
 
 
+def _retagger(epoch, mem, log, name):
+    """The counter warp's retag: not an arrival. It swaps a word with another
+    tag for (epoch << 16) | 0 and leaves a word with this call's tag alone."""
+    cur = mem[0]
+    yield
+    for _ in range(64):
+        if cur >> 16 == epoch:
+            return
+        prev = mem[0]                            # atomicCAS(ctr, cur, epoch << 16)
+        if prev == cur:
+            mem[0] = epoch << 16
+        yield
+        if prev == cur:
+            return
+        cur = prev
+
+
 def _plain_add(epoch, mem, log, name):
     old = mem[0]
     mem[0] = (old + 1) & MASK64
@@ -54,12 +72,14 @@ def _plain_add(epoch, mem, log, name):
     log.append((name, (old & 0xFFFF) + 1))
 
 
-def simulate(seed, n, start, epoch, arrival=_arrival):
+def simulate(seed, n, start, epoch, arrival=_arrival, retaggers=0):
     rnd = random.Random(seed)
     mem = [start]
     log = []
     agents = {i: arrival(epoch, mem, log, i) for i in range(n)}
-    waiting = list(range(n))                     # not started yet
+    for k in range(retaggers):
+        agents[n + k] = _retagger(epoch, mem, log, n + k)
+    waiting = list(agents)                       # not started yet
     running = []
     while waiting or running:
         pick = rnd.randrange(len(waiting) + len(running))
@@ -102,6 +122,21 @@ def test_every_count_once_and_the_word_left_clean(start, n):
             end2, log2 = simulate(seed + 7, n, end, nxt)
             assert sorted(c for _, c in log2) == list(range(1, n + 1))
             assert end2 == nxt << 16
+
+
+@pytest.mark.parametrize("start", list(STARTS), ids=list(STARTS))
+@pytest.mark.parametrize("n", [2, 3, 19])
+def test_early_retag_races_with_arrivals(start, n):
+    """The counter warp retags the word while arrivals may already be adding
+    (a CTA with a one-tile share can reach its segment's end first). Each
+    contributing CTA's counter warp retags, in any interleaving with the
+    adds and swaps: every count 1..n is still handed out once, and the
+    word ends reset."""
+    epoch = 0xBEEF
+    for seed in range(200):
+        end, log = simulate(seed, n, STARTS[start], epoch, retaggers=min(n, 4))
+        assert sorted(c for _, c in log) == list(range(1, n + 1)), (seed, log)
+        assert end == epoch << 16, hex(end)
 
 
 def test_plain_add_miscounts_on_another_calls_word():
