@@ -460,6 +460,33 @@ class DecodeWorkload:
         self.call(stream, self.sets[i % self.copies])
 
 
+def e2e_copy_pairs(dkv, hkv, lens, fp8=False):
+    """(device view, host view) pairs an end-to-end step copies for a
+    contiguous cache: the rows each (sequence, KV head) holds, since the rows
+    past a sequence's length are never read and so are not inputs of the step
+    (for fp8 block scales [B, G, blocks]: the 64-token blocks those rows
+    touch). Runs of sequences whose rows fill the cache are one copy."""
+    pairs = []
+    B = len(lens)
+    for d, h in zip(dkv, hkv):
+        per_block = 64 if (fp8 and h.dim() == 3) else 1
+        G, full = h.shape[1], h.shape[2]
+        rows = [-(-int(t) // per_block) for t in lens]
+        b = 0
+        while b < B:
+            if rows[b] >= full:
+                e = b
+                while e < B and rows[e] >= full:
+                    e += 1
+                pairs.append((d[b:e], h[b:e]))
+                b = e
+                continue
+            if rows[b]:
+                pairs += [(d[b, g, :rows[b]], h[b, g, :rows[b]]) for g in range(G)]
+            b += 1
+    return pairs
+
+
 def _spin(host_us_per_call: float, calls: int):
     """Keeps the stream busy on the device for about as long as the host takes
     to enqueue `calls` more calls (capped at 0.2 s), so that the calls
@@ -604,29 +631,7 @@ def run_gpu(args, cfg):
     else:
         hkv = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in wl.host_kv]
     dkv = wl.sets[0]
-    copies = list(zip(dkv, hkv))
-    if not args.paged:
-        # A contiguous cache is copied as the rows each (sequence, KV head)
-        # holds: the rows past a sequence's length are never read, so they are
-        # not inputs of the step (block scales: the blocks those rows touch).
-        # Runs of sequences whose rows fill the cache are one contiguous copy.
-        copies = []
-        for d, h in zip(dkv, hkv):
-            per_block = 64 if (args.fp8 and h.dim() == 3) else 1
-            full = h.shape[2]
-            b = 0
-            while b < cfg.B:
-                n = -(-int(wl.lens[b]) // per_block)
-                if n >= full:
-                    e = b
-                    while e < cfg.B and -(-int(wl.lens[e]) // per_block) >= full:
-                        e += 1
-                    copies.append((d[b:e], h[b:e]))
-                    b = e
-                    continue
-                if n:
-                    copies += [(d[b, g, :n], h[b, g, :n]) for g in range(cfg.G)]
-                b += 1
+    copies = list(zip(dkv, hkv)) if args.paged else e2e_copy_pairs(dkv, hkv, wl.lens, fp8=args.fp8)
     ho = torch.empty(wl.out.shape, dtype=torch.bfloat16).pin_memory()
     hlse = torch.empty(wl.lse.shape, dtype=torch.float32).pin_memory()
     if args.append:

@@ -10,7 +10,9 @@ the workload it claims to measure.
   n tokens each head sees n(n+1)/2 keys.
 - Launches: one decode kernel per step; a prefill step adds a combine launch
   only when the library splits key ranges (short chunks on a mostly idle GPU).
+- End to end: a step copies the cache rows each sequence holds, nothing more.
 """
+import numpy as np
 import pytest
 
 import bench
@@ -88,3 +90,35 @@ def test_prefill_launches_per_step(monkeypatch):
 def test_percentiles():
     assert bench._percentiles_us([]) is None
     assert bench._percentiles_us([0.001 * i for i in range(1, 12)]) == pytest.approx([2.0, 6.0, 10.0])
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_e2e_copies_cover_exactly_the_valid_rows(fp8):
+    """The end-to-end step copies every row a sequence holds (for fp8 block
+    scales, every 64-token block its rows touch), each once, and nothing past
+    a length; runs of full sequences are single copies."""
+    import torch
+    B, G, Tmax, D = 5, 3, 130, 4
+    lens = np.array([130, 130, 7, 0, 130], dtype=np.int32)
+    host = torch.arange(B * G * Tmax * D, dtype=torch.float32).view(B, G, Tmax, D)
+    dev = torch.zeros_like(host)
+    hkv, dkv = [host], [dev]
+    if fp8:
+        nb = -(-Tmax // 64)
+        hkv.append(torch.arange(B * G * nb, dtype=torch.float32).view(B, G, nb) + 1)
+        dkv.append(torch.zeros(B, G, nb))
+    pairs = bench.e2e_copy_pairs(dkv, hkv, lens, fp8=fp8)
+    for d, h in pairs:
+        d.copy_(h)
+    for b in range(B):
+        n = int(lens[b])
+        assert torch.equal(dev[b, :, :n], host[b, :, :n])
+        assert not dev[b, :, n:].any()
+        if fp8:
+            nbk = -(-n // 64)
+            assert torch.equal(dkv[1][b, :, :nbk], hkv[1][b, :, :nbk])
+            assert not dkv[1][b, :, nbk:].any()
+    full_runs = [p for p in pairs if p[1].dim() == host.dim() and p[1].shape[0] != G]
+    assert [p[1].shape[0] for p in full_runs] == [2, 1]          # sequences 0-1, then 4
+    copied = sum(h.numel() for _, h in pairs if h.dim() >= 2 and h.shape[-1] == D)   # K/V, not scales
+    assert copied == int(lens.sum()) * G * D
