@@ -14,7 +14,8 @@ value    = algorithmic bytes per step / device time per step (GB/s, all ranks);
            the K timed launches are enqueued behind a device-side spin, so the
            events time back-to-back device work, not the binding's call rate
 e2e      = the same with the step's inputs copied from pinned host memory and its
-           outputs copied back inside the timed region
+           outputs copied back inside the timed region (inputs: Q, the lengths and
+           the cache rows each (sequence, KV head) holds; a paged pool whole)
 roofline = the split-KV kernel (the step's only launch): its average duration
            over the timed region, CUDA events on the launching stream,
            against the measured HBM copy bandwidth
